@@ -1,0 +1,414 @@
+"""Benchmark: context-parallel causal GQA prefill attention on GB300.
+
+One step = one ``slope_cp_prefill`` call over the whole workload: every ring
+step's attention launch (partial output + log-sum-exp per rank) followed by
+the exact log-sum-exp merge.  Default workload: S = 32768, 64 query / 8 KV
+heads, head dim 64, bf16, zigzag ring of 8 simulated ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  ``value`` is algorithmic TFLOP/s (visible
+query-key pairs x Hq x 2 x (dqk + dv)) of the whole job; ``e2e`` is the same
+metric measured through the public call with pinned host buffers (host to
+device copies of Q/K/V and device to host copies of out/lse inside the timed
+region).  ``--impl reference`` times the fp64 CPU oracle on a bounded sample
+of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import slope_workloads as wl  # noqa: E402
+
+METRIC = "causal prefill-attention TFLOP/s & tokens/s at 32K–100K; % of GB300 BF16 tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "causal_gqa_s32k_zigzag8"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+K1_SOURCE = os.path.join(ROOT, "ring_attention_slope_gb300", "csrc", "attn_partial.cu")
+
+
+# ---------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def k1_source_hash():
+    with open(K1_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload_name):
+    """DRAM bytes per attention launch from the committed ncu summary, if it is for this kernel source."""
+    path = os.path.join(ROOT, "profiles", f"attn_partial_{workload_name}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_tr or m_hash.group(1) != k1_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def workload_flops(w, window=0):
+    return wl.flops(w, window)
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+
+def oracle_sample(w, target_s, seed=0):
+    """Time the fp64 oracle on a bounded row sample of one KV group; returns (TFLOP/s, seconds, desc, cores)."""
+    import torch
+
+    import oracle
+
+    oracle.build()
+    q, k, v = wl.workload_qkv(w, device="cpu")
+    heads = wl.sample_heads(w)
+    rng = np.random.default_rng(w.seed + 101 + seed)
+    # calibrate on a small sample, then size the timed sample to ~target_s
+    n_rows = 16
+    t_cal = 0.0
+    while True:
+        rows = np.sort(rng.integers(0, w.S, size=n_rows))
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, causal=True, rows=rows, heads=heads)
+        t_cal = time.perf_counter() - t0
+        if t_cal > 0.5 or n_rows >= w.S:
+            break
+        n_rows = min(w.S, n_rows * 4)
+    n_rows = int(min(w.S, max(16, n_rows * target_s / max(t_cal, 1e-3))))
+    rows = np.sort(rng.integers(0, w.S, size=n_rows))
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, causal=True, rows=rows, heads=heads)
+    dt = time.perf_counter() - t0
+    pairs = float(np.sum(rows + 1))  # causal: row i sees i + 1 keys
+    flops = pairs * len(heads) * 2 * (w.dqk + w.dv)
+    desc = (f"{n_rows} random query rows x {len(heads)} heads (one KV group) of {w.name}, "
+            f"causal over all earlier keys; fp64 OpenMP oracle")
+    del torch
+    return flops / dt / 1e12, dt, desc, oracle.num_threads()
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    per_step = max(2.0, min(20.0, 90.0 / max(1, args.steps)))
+    vals, times = [], []
+    for s in range(args.warmup):
+        oracle_sample(w, min(per_step, 2.0), seed=1000 + s)
+    desc, cores = "", 1
+    for s in range(args.steps):
+        v, dt, desc, cores = oracle_sample(w, per_step, seed=s)
+        vals.append(v)
+        times.append(dt)
+    value = float(np.mean(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "dqk": w.dqk, "dv": w.dv,
+                   "layout": w.layout, "n_chunks": wl.n_chunks(w)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_gpu(args, w):
+    import torch
+
+    import ring_attention_slope_gb300 as slope
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    slope.build()
+    slope.load()
+    window = args.window
+    q, k, v = wl.workload_qkv(w, device="cuda")
+    sizes = wl.chunk_sizes(w)
+    n = wl.n_chunks(w)
+    out = torch.empty((w.S, w.Hq, w.dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.Hq, w.S), dtype=torch.float32, device="cuda")
+    ws = torch.empty((slope.cp_prefill_workspace_size(w.S, w.Hq, w.dv, n, w.layout, sizes),), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window, out=out, lse=lse, workspace=ws)
+
+    _, launches_per_step, _ = slope.cp_prefill_plan(w.S, n, w.layout, chunk_sizes=sizes, window=window)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, site = slope.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} at site {site}")
+
+    # ---- timed region: K steps, per-launch events on the launching stream
+    n_pairs = launches_per_step + 8
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_pairs)]
+          for _ in range(args.steps)]
+    for step_ev in ev:
+        for a, b in step_ev:  # materialise the CUDA events
+            a.record(stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.15)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kinds_all, counts = [], []
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for s in range(args.steps):
+        _, _, nl, kinds = slope.cp_prefill_timed(q, k, v, n, w.layout, ev[s], chunk_sizes=sizes, window=window,
+                                                 out=out, lse=lse, workspace=ws)
+        counts.append(nl)
+        kinds_all.append(kinds)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        tt = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    st, site = slope.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} at site {site}")
+
+    k1_ms, k2_ms, k1_n, k2_n = 0.0, 0.0, 0, 0
+    for s in range(args.steps):
+        for i in range(counts[s]):
+            a, b = ev[s][i]
+            d = a.elapsed_time(b)
+            if kinds_all[s][i] == 0:
+                k1_ms += d
+                k1_n += 1
+            else:
+                k2_ms += d
+                k2_n += 1
+
+    flops_step = workload_flops(w, window)
+    value = flops_step * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    tokens_s = w.S * args.steps * world / (elapsed_ms * 1e-3)
+    peaks, peak_src = load_peaks()
+    k1_tflops = flops_step * args.steps / (k1_ms * 1e-3) / 1e12
+    n_planes = n if w.layout != "chunked" else 2
+    # merge: algorithmic bytes = every live partial read once + final out/lse written
+    live_fraction = merge_live_fraction(w, n)
+    merge_bytes = (w.S * w.Hq * (w.dv * 4 + 4) * n_planes * live_fraction + w.S * w.Hq * 4 * n_planes * (1 - live_fraction)
+                   + w.S * w.Hq * (w.dv * 2 + 4))
+    k2_gbs = merge_bytes * k2_n / (k2_ms * 1e-3) / 1e9 if k2_ms > 0 else None
+
+    # ---- end to end through the public call with pinned host buffers
+    e2e = run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier, dist)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "dqk": w.dqk, "dv": w.dv,
+                   "layout": w.layout, "n_chunks": n, "window": window, "batch": 1,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": f"inputs larger than L2 (Q+K+V {q.numel() * 2 + k.numel() * 2 + v.numel() * 2} B, "
+                         f"partials {ws.numel()} B > {L2_BYTES} B); no flush",
+                   "flops_per_step": flops_step},
+        "tokens_per_s": tokens_s,
+        "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],
+        "roofline": {"bound": "tensor", "achieved": k1_tflops, "peak": peaks["bf16_tflops_sustained"],
+                     "unit": "TFLOP/s", "frac": k1_tflops / peaks["bf16_tflops_sustained"],
+                     "traffic": profiled_traffic(w.name), "kernel": "attn_partial_kernel",
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a multi-launch step)",
+                     "launches": k1_n, "avg_launch_ms": k1_ms / max(1, k1_n)},
+        "roofline_merge": {"bound": "hbm", "achieved": k2_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": (k2_gbs / peaks["hbm_gbs"]) if k2_gbs else None,
+                           "bytes_per_launch": merge_bytes, "kernel": "lse_merge_kernel",
+                           "avg_launch_ms": k2_ms / max(1, k2_n)},
+        "e2e": e2e,
+        "gpu_launches": int(sum(counts)),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v_cpu, dt, desc, cores = oracle_sample(w, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+                                  "seconds": dt}
+    if rank == 0:
+        print(json.dumps(result))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def merge_live_fraction(w, n):
+    """Fraction of (row, plane) partials that hold a visible key (the merge reads only those)."""
+    if w.layout == "chunked":
+        sizes = wl.chunk_sizes(w)
+        return 1.0 - sizes[0] / w.S / 2.0  # chunk 0 has no prefix partial
+    if w.layout == "zigzag":
+        # early sub-chunk r sees r + 1 of the N steps, late sub-chunks see all N
+        return (sum(r + 1 for r in range(n)) + n * n) / (2 * n * n)
+    return (n + 1) / (2 * n)
+
+
+def run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier, dist):
+    hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    hk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
+    hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+    hq.copy_(q)
+    hk.copy_(k)
+    hv.copy_(v)
+    ho = torch.empty((w.S, w.Hq, w.dv), dtype=torch.bfloat16, pin_memory=True)
+    hl = torch.empty((w.Hq, w.S), dtype=torch.float32, pin_memory=True)
+    dq, dk, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    out = torch.empty((w.S, w.Hq, w.dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.Hq, w.S), dtype=torch.float32, device="cuda")
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        slope.cp_prefill(dq, dk, dv_, n, w.layout, chunk_sizes=sizes, window=window, out=out, lse=lse,
+                         workspace=ws)
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    world = 1
+    if dist is not None:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        world = dist.get_world_size()
+    val = workload_flops(w, window) * args.steps * world / (ms * 1e-3) / 1e12
+    return {"value": val, "unit": UNIT, "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
+            "d2h_bytes_per_step": int(ho.numel() * 2 + hl.numel() * 4), "ms_per_step": ms / args.steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["slope", "reference"], default="slope")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.BY_NAME))
+    ap.add_argument("--window", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    w = wl.BY_NAME[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,223 @@
+/*
+ * slope.h - C ABI of libslope: context-parallel causal GQA prefill attention
+ * on one GB300 (sm_103a).
+ *
+ * The method: the SLOPE prefill engine (Moreh, "Optimizing long-context
+ * prefill on multiple older-generation GPU nodes", section "Introduction to
+ * Context Parallelism") splits a prompt along the sequence dimension; every op
+ * but attention is per-token, and attention is computed by Ring Attention:
+ * each device attends its share of the queries to the key/value block it
+ * currently holds while key/value blocks circulate between neighbours.  The
+ * SGLang pipeline-parallelism article ("SGLang Pipeline Parallelism: 1M-token
+ * context ...", TL;DR) processes long prompts as chunked prefill with
+ * 12K-token chunks, each chunk attending to the growing key/value prefix.
+ *
+ * This library computes exactly that attention on one GPU: the ring's steps
+ * (or the chunks) run in order, each step emitting a partial output plus its
+ * log-sum-exp, and the partials are combined by an exact log-sum-exp merge.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensors are described by slope_tensor: a DEVICE pointer, a dtype, a rank
+ *    and shape/stride in ELEMENTS.  The innermost stride must be 1.
+ *  - Q is [Sq, Hq, dqk], K is [Skv, Hkv, dqk], V is [Skv, Hkv, dv], all bf16,
+ *    token-major (batch 1).  Row and head strides of Q/K/V must be multiples
+ *    of 8 elements (16 bytes) and the data pointer 16-byte aligned, because
+ *    the kernels read them with the Tensor Memory Accelerator.
+ *  - Supported head sizes (dqk, dv): (64, 64), (128, 64), (128, 128) and
+ *    (192, 128); other pairs return SLOPE_ERR_UNSUPPORTED.  Hq must be a
+ *    multiple of Hkv; query head h reads key/value head h / (Hq / Hkv).
+ *  - Masks use GLOBAL token positions: key j is visible to query i iff
+ *    (!causal || pos(j) <= pos(i)) && (window == 0 || pos(i) - pos(j) < window).
+ *  - scale <= 0 selects 1/sqrt(dqk).  lse is the natural log of the sum of
+ *    exp(scale * q.k) over the visible keys.  A query row that sees no key
+ *    gets out = 0 and lse = -inf (never NaN).
+ *  - The library never allocates or frees device memory; the caller owns
+ *    every buffer, including the workspace.  Host arrays passed in are read
+ *    during the call only.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and does not synchronise.  Argument errors are returned
+ *    before anything is launched and leave the outputs untouched; a failed
+ *    launch returns SLOPE_ERR_CUDA.  Kernel waits are bounded: a wait that
+ *    runs out records SLOPE_ERR_TIMEOUT in a device status word that
+ *    slope_device_status() reports.
+ *  - Calls are thread-safe (no mutable library state besides the device
+ *    status word and a lazily resolved driver entry point).
+ */
+#ifndef SLOPE_H
+#define SLOPE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SLOPE_API __attribute__((visibility("default")))
+#else
+#define SLOPE_API
+#endif
+
+typedef enum {
+  SLOPE_OK = 0,
+  SLOPE_ERR_NULL = -1,        /* a required pointer is NULL                         */
+  SLOPE_ERR_DTYPE = -2,       /* wrong element type                                 */
+  SLOPE_ERR_SHAPE = -3,       /* inconsistent or unsupported shape                  */
+  SLOPE_ERR_STRIDE = -4,      /* innermost stride != 1, or misaligned stride/pointer */
+  SLOPE_ERR_LAYOUT = -5,      /* layout/chunking does not divide the sequence        */
+  SLOPE_ERR_CUDA = -6,        /* a CUDA runtime/driver call failed                   */
+  SLOPE_ERR_TIMEOUT = -7,     /* a bounded device wait ran out                       */
+  SLOPE_ERR_UNSUPPORTED = -8, /* valid request outside what the kernels implement    */
+  SLOPE_ERR_WORKSPACE = -9    /* workspace missing, too small or misaligned          */
+} slope_status;
+
+typedef enum { SLOPE_BF16 = 0, SLOPE_F32 = 1 } slope_dtype;
+
+typedef struct {
+  void* data;        /* device pointer                                */
+  slope_dtype dtype; /* element type                                  */
+  int32_t ndim;      /* 2 or 3                                        */
+  int64_t shape[3];  /* sizes, outermost first                        */
+  int64_t stride[3]; /* strides in elements; stride[ndim-1] must be 1 */
+} slope_tensor;
+
+typedef enum {
+  SLOPE_LAYOUT_CONTIGUOUS = 0, /* ring of n ranks, rank r owns tokens [r*S/n, (r+1)*S/n)          */
+  SLOPE_LAYOUT_ZIGZAG = 1,     /* ring of n ranks, rank r owns sub-chunks r and 2n-1-r of S/(2n)  */
+  SLOPE_LAYOUT_CHUNKED = 2     /* chunked prefill: chunk c attends to all earlier tokens + itself */
+} slope_layout;
+
+/*
+ * Partial attention of one query block against one key/value block
+ * (Ring Attention item: a device attends its partial queries to the partial
+ * keys/values it holds).
+ *
+ *   q   bf16 [Sq, Hq, dqk]    k bf16 [Skv, Hkv, dqk]    v bf16 [Skv, Hkv, dv]
+ *   q_off / kv_off: global positions of q row 0 / k row 0 (the masks use them).
+ *   causal, window, scale: see the conventions above.
+ *   out fp32 [Sq, Hq, dv]: the softmax-normalised output over the visible keys
+ *       of this block (0 for rows that see none).  Innermost stride 1, row and
+ *       head strides multiples of 4 elements, pointer 16-byte aligned.
+ *   lse fp32, rank 2 [Hq, Sq] (any strides): natural-log log-sum-exp of the
+ *       scaled scores over the visible keys of this block (-inf if none).
+ * Sq == 0 is a no-op.  Returns SLOPE_OK or an error status.
+ */
+SLOPE_API slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v,
+                                int64_t q_off, int64_t kv_off, int causal, int64_t window, float scale,
+                                slope_tensor* out, slope_tensor* lse, void* stream);
+
+/*
+ * Exact log-sum-exp merge of n partials computed over disjoint key sets
+ * (the combination step of Ring Attention):
+ *   L   = log sum_k exp(lse_k)            (max-shifted; all -inf gives -inf)
+ *   out = sum_k exp(lse_k - L) * out_k     (partials with lse_k = -inf are skipped)
+ *
+ *   outs[k] fp32 [S, H, dv], lses[k] fp32 rank 2 [H, S] (any strides), 1 <= n <= 32.
+ *   out: bf16 or fp32 [S, H, dv] (innermost stride 1, row/head strides multiples
+ *        of 4 elements, 16-byte aligned pointers for out and every outs[k]).
+ *   lse: fp32 [H, S], or NULL to skip writing it.
+ * `outs` and `lses` are host arrays of n descriptors.
+ */
+SLOPE_API slope_status slope_lse_merge(const slope_tensor* outs, const slope_tensor* lses, int n, slope_tensor* out,
+                             slope_tensor* lse, void* stream);
+
+/*
+ * Whole context-parallel prefill attention of one layer on one GPU.
+ *
+ *   q bf16 [S, Hq, dqk], k bf16 [S, Hkv, dqk], v bf16 [S, Hkv, dv] (positions 0..S-1).
+ *   layout SLOPE_LAYOUT_CONTIGUOUS / SLOPE_LAYOUT_ZIGZAG: a ring of n_chunks
+ *     simulated ranks.  At ring step t rank r holds the keys/values of rank
+ *     (r - t) mod n_chunks; each step is ONE attention-kernel launch covering
+ *     every rank, writing one partial per (rank, step); a final merge launch
+ *     combines each row's partials.  CONTIGUOUS needs S % n_chunks == 0,
+ *     ZIGZAG needs S % (2*n_chunks) == 0.  1 <= n_chunks <= 32.
+ *   layout SLOPE_LAYOUT_CHUNKED: n_chunks query chunks, sizes chunk_sizes[0..n)
+ *     (summing to S), or NULL for ceil(S/n_chunks) with a shorter last chunk.
+ *     Chunk [s, e) yields two partials - against keys [0, s) and, causally,
+ *     against [s, e) - computed in one launch per chunk, in order, then merged.
+ *   causal, window, scale: as above.  out: bf16 or fp32 [S, Hq, dv];
+ *   lse: fp32 [Hq, S] or NULL.
+ *   workspace: device buffer of at least slope_cp_prefill_workspace_size()
+ *     bytes, 256-byte aligned; it holds the fp32 partials between the
+ *     attention launches and the merge.
+ */
+SLOPE_API slope_status slope_cp_prefill(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
+                              slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
+                              float scale, slope_tensor* out, slope_tensor* lse, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Workspace bytes slope_cp_prefill needs for these sizes (0 on invalid arguments). */
+SLOPE_API size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t dv, int n_chunks, slope_layout layout,
+                                       const int64_t* chunk_sizes);
+
+/*
+ * Same as slope_cp_prefill, and additionally records a pair of CUDA events
+ * around every kernel launch it makes, on `stream`: events[2*i] before launch
+ * i and events[2*i+1] after it.  events is a host array of 2*n_event_pairs
+ * cudaEvent_t handles created by the caller.  On return *n_launches holds the
+ * number of launches made and launch_kind[i] (if non-NULL, n_event_pairs
+ * entries) is 0 for an attention-partial launch and 1 for the merge.
+ * Returns SLOPE_ERR_SHAPE if n_event_pairs is smaller than the launch count.
+ */
+SLOPE_API slope_status slope_cp_prefill_timed(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v,
+                                    int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
+                                    int64_t window, float scale, slope_tensor* out, slope_tensor* lse,
+                                    void* workspace, size_t workspace_bytes, void* stream, void** events,
+                                    int n_event_pairs, int* n_launches, int* launch_kind);
+
+/*
+ * Host-only view of the work decomposition slope_cp_prefill performs (no GPU
+ * needed).  One entry per (launch, query block): the query rows, the partial
+ * plane written and the key/value row ranges attended in that launch
+ * (after dropping blocks the mask hides entirely).
+ */
+typedef struct {
+  int32_t launch;     /* attention launch index (ring step or chunk)      */
+  int32_t plane;      /* partial plane written                             */
+  int64_t q_row0;     /* first query row                                   */
+  int64_t q_len;      /* number of query rows                              */
+  int32_t n_kv;       /* number of key/value ranges (0..2)                 */
+  int64_t kv_row0[2]; /* first key row of each range                       */
+  int64_t kv_len[2];  /* length of each range                              */
+} slope_plan_item;
+
+/*
+ * Fills up to `capacity` items (items may be NULL when capacity is 0) and
+ * returns the total number of items, or a negative slope_status.  *n_launches
+ * and *n_planes (if non-NULL) receive the attention-launch and partial-plane
+ * counts.
+ */
+SLOPE_API int64_t slope_cp_prefill_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes,
+                              int causal, int64_t window, slope_plan_item* items, int64_t capacity,
+                              int32_t* n_launches, int32_t* n_planes);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device: SLOPE_OK, or SLOPE_ERR_TIMEOUT if a bounded kernel wait ran
+ * out since the last query (the kernel that saw it skipped its remaining work
+ * and released its tensor memory).  *site (if non-NULL) receives the code of
+ * the wait that ran out (0 when none).
+ */
+SLOPE_API slope_status slope_device_status(void* stream, int* site);
+
+/*
+ * Self-test of the bounded-wait path: launches one block that waits on a
+ * barrier nothing will ever complete, with the given limit in nanoseconds
+ * (1e3..5e9).  The wait runs out, records SLOPE_ERR_TIMEOUT in the device
+ * status word and the kernel returns normally; no fault, no hang.
+ */
+SLOPE_API slope_status slope_debug_timeout_selftest(uint64_t limit_ns, void* stream);
+
+/* Static description of a status code. */
+SLOPE_API const char* slope_status_string(slope_status s);
+
+/* Library version string. */
+SLOPE_API const char* slope_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SLOPE_H */

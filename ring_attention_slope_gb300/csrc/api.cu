@@ -1,0 +1,629 @@
+// C ABI of libslope (declared in include/slope.h): argument validation, the
+// work decomposition of context-parallel prefill, TMA tensor maps and the
+// kernel launches.  The library allocates no device memory.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "kernels.cuh"
+#include "slope.h"
+
+using namespace slope;
+
+namespace {
+
+constexpr int kMaxRanks = 32;
+constexpr int64_t kMaxSeq = int64_t(1) << 30;
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+
+// ---------------------------------------------------------------- argument checks
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// bf16 [S, H, d] readable by TMA: innermost stride 1, other strides multiples of 8 elements.
+slope_status check_qkv(const slope_tensor* t) {
+  if (t == nullptr) return SLOPE_ERR_NULL;
+  if (t->dtype != SLOPE_BF16) return SLOPE_ERR_DTYPE;
+  if (t->ndim != 3) return SLOPE_ERR_SHAPE;
+  if (t->shape[0] < 0 || t->shape[1] <= 0 || t->shape[2] <= 0 || t->shape[0] > kMaxSeq || t->shape[1] > 65535)
+    return SLOPE_ERR_SHAPE;
+  if (t->shape[0] > 0 && t->data == nullptr) return SLOPE_ERR_NULL;
+  if (t->stride[2] != 1) return SLOPE_ERR_STRIDE;
+  if (t->stride[0] <= 0 || t->stride[1] <= 0 || t->stride[0] % 8 || t->stride[1] % 8) return SLOPE_ERR_STRIDE;
+  if (!aligned(t->data, 16)) return SLOPE_ERR_STRIDE;
+  return SLOPE_OK;
+}
+
+// [S, H, dv] output, fp32 (or bf16 when allowed); 16-byte vector stores.
+slope_status check_out(const slope_tensor* t, int64_t S, int64_t H, int64_t dv, bool allow_bf16) {
+  if (t == nullptr) return SLOPE_ERR_NULL;
+  if (t->dtype != SLOPE_F32 && !(allow_bf16 && t->dtype == SLOPE_BF16)) return SLOPE_ERR_DTYPE;
+  if (t->ndim != 3 || t->shape[0] != S || t->shape[1] != H || t->shape[2] != dv) return SLOPE_ERR_SHAPE;
+  if (S > 0 && t->data == nullptr) return SLOPE_ERR_NULL;
+  if (t->stride[2] != 1 || t->stride[0] <= 0 || t->stride[1] <= 0) return SLOPE_ERR_STRIDE;
+  if (t->stride[0] % 4 || t->stride[1] % 4) return SLOPE_ERR_STRIDE;
+  if (!aligned(t->data, t->dtype == SLOPE_F32 ? 16 : 8)) return SLOPE_ERR_STRIDE;
+  return SLOPE_OK;
+}
+
+// fp32 [H, S], any positive strides.
+slope_status check_lse(const slope_tensor* t, int64_t H, int64_t S) {
+  if (t == nullptr) return SLOPE_ERR_NULL;
+  if (t->dtype != SLOPE_F32) return SLOPE_ERR_DTYPE;
+  if (t->ndim != 2 || t->shape[0] != H || t->shape[1] != S) return SLOPE_ERR_SHAPE;
+  if (S > 0 && t->data == nullptr) return SLOPE_ERR_NULL;
+  if (t->stride[0] <= 0 || t->stride[1] <= 0) return SLOPE_ERR_STRIDE;
+  if (!aligned(t->data, 4)) return SLOPE_ERR_STRIDE;
+  return SLOPE_OK;
+}
+
+uint64_t wait_limit_ns() {
+  static const uint64_t limit = [] {
+    const char* e = std::getenv("SLOPE_WAIT_LIMIT_NS");
+    if (e != nullptr) {
+      const unsigned long long v = std::strtoull(e, nullptr, 10);
+      if (v >= 1000ull && v <= 60000000000ull) return static_cast<uint64_t>(v);
+    }
+    return kDefaultWaitLimitNs;
+  }();
+  return limit;
+}
+
+float resolve_scale(float scale, int64_t dqk) {
+  return scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(dqk)));
+}
+
+// ---------------------------------------------------------------- TMA tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// 3-D view {d, H, S} of a bf16 [S, H, d] tensor; box = 64 columns x 1 head x 128 rows,
+// 128-byte swizzle (the layout the tcgen05 descriptors expect); out-of-range rows read 0.
+bool make_map(CUtensorMap* m, const slope_tensor* t) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  std::memset(m, 0, sizeof(*m));
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(t->shape[2]), static_cast<cuuint64_t>(t->shape[1]),
+                        static_cast<cuuint64_t>(t->shape[0])};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(t->stride[1]) * 2, static_cast<cuuint64_t>(t->stride[0]) * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBlockN)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, t->data, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- work decomposition
+
+struct Range {
+  int64_t row0, len;
+};
+struct PItem {
+  int launch, plane;
+  int64_t q_row0, q_len;
+  int n_kv;
+  Range kv[kMaxKvRanges];
+};
+struct Plan {
+  std::vector<PItem> items;  // grouped by launch, in launch order
+  int n_launches = 0;
+  int n_planes = 0;
+};
+
+// Restricts keys [k0, k1) to those some query in [q0, q1) can see (positions = rows).
+bool trim(int64_t q0, int64_t q1, int64_t& k0, int64_t& k1, int causal, int64_t window) {
+  if (causal) k1 = std::min(k1, q1);
+  if (window > 0) k0 = std::max(k0, q0 - window + 1);
+  return k1 > k0;
+}
+
+slope_status chunk_list(int64_t S, int n_chunks, const int64_t* chunk_sizes, std::vector<int64_t>& sizes) {
+  sizes.clear();
+  if (n_chunks < 1 || n_chunks > 4096) return SLOPE_ERR_LAYOUT;
+  if (chunk_sizes != nullptr) {
+    int64_t sum = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      if (chunk_sizes[c] <= 0) return SLOPE_ERR_LAYOUT;
+      sum += chunk_sizes[c];
+      sizes.push_back(chunk_sizes[c]);
+    }
+    if (sum != S) return SLOPE_ERR_LAYOUT;
+  } else {
+    const int64_t c = (S + n_chunks - 1) / n_chunks;
+    int64_t left = S;
+    for (int i = 0; i < n_chunks; ++i) {
+      const int64_t sz = std::min(c, left);
+      if (sz <= 0) return SLOPE_ERR_LAYOUT;
+      sizes.push_back(sz);
+      left -= sz;
+    }
+  }
+  return SLOPE_OK;
+}
+
+// Ring layouts: at step t rank r holds the keys/values of rank (r - t) mod N; each
+// of r's query sub-chunks attends to the visible parts of those sub-chunks and
+// writes partial plane t.  Chunked: chunk [s, e) gives (Q_c, KV[0, s)) -> plane 0
+// and (Q_c, KV[s, e)) -> plane 1, one launch per chunk.
+slope_status build_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
+                        int64_t window, Plan& plan) {
+  plan = Plan();
+  if (S <= 0 || S > kMaxSeq) return SLOPE_ERR_SHAPE;
+  if (window < 0) return SLOPE_ERR_SHAPE;
+  if (layout == SLOPE_LAYOUT_CONTIGUOUS || layout == SLOPE_LAYOUT_ZIGZAG) {
+    const int N = n_chunks;
+    if (N < 1 || N > kMaxRanks) return SLOPE_ERR_LAYOUT;
+    const bool zz = layout == SLOPE_LAYOUT_ZIGZAG;
+    const int64_t parts = zz ? 2 * N : N;
+    if (S % parts != 0) return SLOPE_ERR_LAYOUT;
+    const int64_t sub = S / parts;
+    auto owned = [&](int r, int64_t* out) -> int {
+      out[0] = r;
+      if (!zz) return 1;
+      out[1] = 2 * N - 1 - r;
+      return 2;
+    };
+    for (int t = 0; t < N; ++t) {
+      for (int r = 0; r < N; ++r) {
+        const int src = ((r - t) % N + N) % N;
+        int64_t qa[2], kb[2];
+        const int nq = owned(r, qa), nk = owned(src, kb);
+        for (int i = 0; i < nq; ++i) {
+          PItem it{};
+          it.launch = t;
+          it.plane = t;
+          it.q_row0 = qa[i] * sub;
+          it.q_len = sub;
+          it.n_kv = 0;
+          for (int j = 0; j < nk; ++j) {
+            int64_t k0 = kb[j] * sub, k1 = k0 + sub;
+            if (trim(it.q_row0, it.q_row0 + sub, k0, k1, causal, window)) it.kv[it.n_kv++] = Range{k0, k1 - k0};
+          }
+          plan.items.push_back(it);
+        }
+      }
+    }
+    plan.n_launches = N;
+    plan.n_planes = N;
+    return SLOPE_OK;
+  }
+  if (layout == SLOPE_LAYOUT_CHUNKED) {
+    std::vector<int64_t> sizes;
+    slope_status st = chunk_list(S, n_chunks, chunk_sizes, sizes);
+    if (st != SLOPE_OK) return st;
+    int64_t s0 = 0;
+    for (size_t c = 0; c < sizes.size(); ++c) {
+      const int64_t s1 = s0 + sizes[c];
+      PItem pre{}, own{};
+      pre.launch = own.launch = static_cast<int>(c);
+      pre.plane = 0;
+      own.plane = 1;
+      pre.q_row0 = own.q_row0 = s0;
+      pre.q_len = own.q_len = s1 - s0;
+      int64_t k0 = 0, k1 = s0;
+      if (trim(s0, s1, k0, k1, causal, window)) pre.kv[pre.n_kv++] = Range{k0, k1 - k0};
+      k0 = s0;
+      k1 = s1;
+      if (trim(s0, s1, k0, k1, causal, window)) own.kv[own.n_kv++] = Range{k0, k1 - k0};
+      plan.items.push_back(pre);
+      plan.items.push_back(own);
+      s0 = s1;
+    }
+    plan.n_launches = static_cast<int>(sizes.size());
+    plan.n_planes = 2;
+    return SLOPE_OK;
+  }
+  return SLOPE_ERR_LAYOUT;
+}
+
+// Rough work estimate (visible pairs) used to order items heaviest first.
+double item_work(const PItem& it, int causal) {
+  double w = 0;
+  for (int r = 0; r < it.n_kv; ++r) {
+    const bool diag = causal && it.kv[r].row0 + it.kv[r].len > it.q_row0;
+    w += static_cast<double>(it.q_len) * static_cast<double>(it.kv[r].len) * (diag ? 0.5 : 1.0);
+  }
+  return w;
+}
+
+// Packs items into launch parameter blocks (<= kMaxItems each), heaviest first.
+void pack_items(std::vector<PItem> items, int causal, std::vector<std::vector<WorkItem>>& out) {
+  std::stable_sort(items.begin(), items.end(),
+                   [&](const PItem& a, const PItem& b) { return item_work(a, causal) > item_work(b, causal); });
+  out.clear();
+  for (size_t i = 0; i < items.size(); i += kMaxItems) {
+    std::vector<WorkItem> group;
+    int32_t begin = 0;
+    for (size_t j = i; j < std::min(items.size(), i + kMaxItems); ++j) {
+      const PItem& s = items[j];
+      WorkItem w{};
+      w.q_row0 = static_cast<int32_t>(s.q_row0);
+      w.q_len = static_cast<int32_t>(s.q_len);
+      w.out_row0 = static_cast<int32_t>(s.q_row0);
+      w.plane = s.plane;
+      w.n_kv = s.n_kv;
+      for (int r = 0; r < s.n_kv; ++r) w.kv[r] = KvRange{static_cast<int32_t>(s.kv[r].row0),
+                                                        static_cast<int32_t>(s.kv[r].len)};
+      w.n_blocks = static_cast<int32_t>((s.q_len + kRowsPerCta - 1) / kRowsPerCta);
+      w.cta_begin = begin;
+      begin += w.n_blocks;
+      group.push_back(w);
+    }
+    out.push_back(std::move(group));
+  }
+}
+
+// ---------------------------------------------------------------- launches
+
+struct Timing {
+  void** events = nullptr;
+  int capacity = 0;
+  int count = 0;
+  int* kinds = nullptr;
+};
+
+cudaError_t record(Timing* tm, bool before, int kind, cudaStream_t stream) {
+  if (tm == nullptr) return cudaSuccess;
+  if (before) {
+    if (tm->count >= tm->capacity) return cudaErrorInvalidValue;
+    if (tm->kinds != nullptr) tm->kinds[tm->count] = kind;
+    return cudaEventRecord(static_cast<cudaEvent_t>(tm->events[2 * tm->count]), stream);
+  }
+  cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(tm->events[2 * tm->count + 1]), stream);
+  ++tm->count;
+  return e;
+}
+
+slope_status run_attention(const std::vector<WorkItem>& group, int dqk, int dv, const CUtensorMap& tq,
+                           const CUtensorMap& tk, const CUtensorMap& tv, AttnParams base, Timing* tm,
+                           cudaStream_t stream) {
+  base.n_items = static_cast<int32_t>(group.size());
+  for (size_t i = 0; i < group.size(); ++i) base.items[i] = group[i];
+  if (record(tm, true, 0, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
+  if (launch_attn_partial(dqk, dv, tq, tk, tv, base, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
+  if (record(tm, false, 0, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
+  return SLOPE_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WorkspaceLayout {
+  size_t out_bytes, lse_offset, total;
+};
+WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t dv, int n_planes) {
+  WorkspaceLayout w;
+  w.out_bytes = static_cast<size_t>(S) * Hq * dv * sizeof(float);
+  w.lse_offset = round_up(w.out_bytes * n_planes, 256);
+  w.total = w.lse_offset + round_up(static_cast<size_t>(S) * Hq * sizeof(float) * n_planes, 256);
+  return w;
+}
+
+slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
+                             slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
+                             float scale, slope_tensor* out, slope_tensor* lse, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream, Timing* tm) {
+  slope_status st;
+  if ((st = check_qkv(q)) != SLOPE_OK || (st = check_qkv(k)) != SLOPE_OK || (st = check_qkv(v)) != SLOPE_OK)
+    return st;
+  const int64_t S = q->shape[0], Hq = q->shape[1], dqk = q->shape[2];
+  const int64_t Hkv = k->shape[1], dv = v->shape[2];
+  if (k->shape[0] != S || v->shape[0] != S || v->shape[1] != Hkv || k->shape[2] != dqk) return SLOPE_ERR_SHAPE;
+  if (Hq % Hkv != 0) return SLOPE_ERR_SHAPE;
+  if (!attn_partial_supported(static_cast<int>(dqk), static_cast<int>(dv))) return SLOPE_ERR_UNSUPPORTED;
+  if (window < 0 || window > kMaxSeq) return SLOPE_ERR_SHAPE;
+  if ((st = check_out(out, S, Hq, dv, true)) != SLOPE_OK) return st;
+  if (lse != nullptr && (st = check_lse(lse, Hq, S)) != SLOPE_OK) return st;
+  if (S == 0) return SLOPE_ERR_SHAPE;
+  Plan plan;
+  if ((st = build_plan(S, n_chunks, layout, chunk_sizes, causal, window, plan)) != SLOPE_OK) return st;
+  if (plan.n_planes > kMaxMerge) return SLOPE_ERR_UNSUPPORTED;
+  const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes);
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < wl.total) return SLOPE_ERR_WORKSPACE;
+  int* status = device_status_ptr();
+  if (status == nullptr) return SLOPE_ERR_CUDA;
+
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q) || !make_map(&tk, k) || !make_map(&tv, v)) return SLOPE_ERR_CUDA;
+
+  float* planes = static_cast<float*>(workspace);
+  float* lse_planes = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.lse_offset);
+  AttnParams base{};
+  base.Hq = static_cast<int32_t>(Hq);
+  base.group = static_cast<int32_t>(Hq / Hkv);
+  base.causal = causal ? 1 : 0;
+  base.window = static_cast<int32_t>(window);
+  base.q_pos_off = 0;
+  base.kv_pos_off = 0;
+  base.write_empty_out = 0;  // the merge never reads partials whose lse is -inf
+  base.scale_log2 = resolve_scale(scale, dqk) * 1.44269504088896340736f;
+  base.out = planes;
+  base.out_srow = Hq * dv;
+  base.out_shead = dv;
+  base.out_splane = S * Hq * dv;
+  base.lse = lse_planes;
+  base.lse_srow = Hq;
+  base.lse_shead = 1;
+  base.lse_splane = S * Hq;
+  base.status = status;
+  base.wait_limit_ns = wait_limit_ns();
+
+  // One or more launches per ring step / chunk, in order.
+  size_t i = 0;
+  std::vector<std::vector<WorkItem>> groups;
+  for (int l = 0; l < plan.n_launches; ++l) {
+    std::vector<PItem> items;
+    while (i < plan.items.size() && plan.items[i].launch == l) items.push_back(plan.items[i++]);
+    pack_items(items, causal, groups);
+    for (const auto& g : groups)
+      if ((st = run_attention(g, static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, base, tm, stream)) !=
+          SLOPE_OK)
+        return st;
+  }
+
+  MergeParams mp{};
+  mp.n = plan.n_planes;
+  mp.H = static_cast<int32_t>(Hq);
+  mp.dv = static_cast<int32_t>(dv);
+  mp.S = S;
+  for (int pl = 0; pl < plan.n_planes; ++pl) {
+    mp.outs[pl] = planes + static_cast<int64_t>(pl) * S * Hq * dv;
+    mp.lses[pl] = lse_planes + static_cast<int64_t>(pl) * S * Hq;
+    mp.o_srow[pl] = Hq * dv;
+    mp.o_shead[pl] = dv;
+    mp.l_srow[pl] = Hq;
+    mp.l_shead[pl] = 1;
+  }
+  mp.out = out->data;
+  mp.out_bf16 = out->dtype == SLOPE_BF16 ? 1 : 0;
+  mp.out_srow = out->stride[0];
+  mp.out_shead = out->stride[1];
+  mp.lse = lse != nullptr ? static_cast<float*>(lse->data) : nullptr;
+  mp.lse_srow = lse != nullptr ? lse->stride[1] : 0;
+  mp.lse_shead = lse != nullptr ? lse->stride[0] : 0;
+  if (record(tm, true, 1, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
+  if (launch_lse_merge(mp, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
+  if (record(tm, false, 1, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
+  return SLOPE_OK;
+}
+
+}  // namespace
+
+// ==================================================================== exported
+
+extern "C" {
+
+slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int64_t q_off,
+                                int64_t kv_off, int causal, int64_t window, float scale, slope_tensor* out,
+                                slope_tensor* lse, void* stream) {
+  slope_status st;
+  if ((st = check_qkv(q)) != SLOPE_OK) return st;
+  if (k == nullptr || v == nullptr) return SLOPE_ERR_NULL;
+  if (k->dtype != SLOPE_BF16 || v->dtype != SLOPE_BF16) return SLOPE_ERR_DTYPE;
+  if (k->ndim != 3 || v->ndim != 3) return SLOPE_ERR_SHAPE;
+  const int64_t Sq = q->shape[0], Hq = q->shape[1], dqk = q->shape[2];
+  const int64_t Skv = k->shape[0], Hkv = k->shape[1], dv = v->shape[2];
+  if (Skv > 0) {
+    if ((st = check_qkv(k)) != SLOPE_OK || (st = check_qkv(v)) != SLOPE_OK) return st;
+  } else if (k->shape[1] <= 0 || v->shape[1] <= 0 || v->shape[2] <= 0 || k->shape[0] < 0) {
+    return SLOPE_ERR_SHAPE;
+  }
+  if (v->shape[0] != Skv || v->shape[1] != Hkv || k->shape[2] != dqk) return SLOPE_ERR_SHAPE;
+  if (Hq % Hkv != 0) return SLOPE_ERR_SHAPE;
+  if (!attn_partial_supported(static_cast<int>(dqk), static_cast<int>(dv))) return SLOPE_ERR_UNSUPPORTED;
+  if (window < 0 || window > kMaxSeq) return SLOPE_ERR_SHAPE;
+  if (std::llabs(q_off) > kMaxSeq || std::llabs(kv_off) > kMaxSeq) return SLOPE_ERR_SHAPE;
+  if ((st = check_out(out, Sq, Hq, dv, false)) != SLOPE_OK) return st;
+  if ((st = check_lse(lse, Hq, Sq)) != SLOPE_OK) return st;
+  if (Sq == 0) return SLOPE_OK;
+  int* status = device_status_ptr();
+  if (status == nullptr) return SLOPE_ERR_CUDA;
+
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q)) return SLOPE_ERR_CUDA;
+  if (Skv > 0) {
+    if (!make_map(&tk, k) || !make_map(&tv, v)) return SLOPE_ERR_CUDA;
+  } else {
+    tk = tq;  // never read: an item with no key range issues no K/V load
+    tv = tq;
+  }
+  PItem it{};
+  it.q_row0 = 0;
+  it.q_len = Sq;
+  it.plane = 0;
+  it.n_kv = 0;
+  if (Skv > 0) {
+    // positions of the query block / key block
+    int64_t k0 = kv_off, k1 = kv_off + Skv;
+    if (trim(q_off, q_off + Sq, k0, k1, causal, window)) it.kv[it.n_kv++] = Range{k0 - kv_off, k1 - k0};
+  }
+  std::vector<std::vector<WorkItem>> groups;
+  pack_items({it}, causal, groups);
+
+  AttnParams base{};
+  base.Hq = static_cast<int32_t>(Hq);
+  base.group = static_cast<int32_t>(Hq / Hkv);
+  base.causal = causal ? 1 : 0;
+  base.window = static_cast<int32_t>(window);
+  base.q_pos_off = static_cast<int32_t>(q_off);
+  base.kv_pos_off = static_cast<int32_t>(kv_off);
+  base.write_empty_out = 1;
+  base.scale_log2 = resolve_scale(scale, dqk) * 1.44269504088896340736f;
+  base.out = static_cast<float*>(out->data);
+  base.out_srow = out->stride[0];
+  base.out_shead = out->stride[1];
+  base.out_splane = 0;
+  base.lse = static_cast<float*>(lse->data);
+  base.lse_srow = lse->stride[1];
+  base.lse_shead = lse->stride[0];
+  base.lse_splane = 0;
+  base.status = status;
+  base.wait_limit_ns = wait_limit_ns();
+  return run_attention(groups[0], static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, base, nullptr,
+                       static_cast<cudaStream_t>(stream));
+}
+
+slope_status slope_lse_merge(const slope_tensor* outs, const slope_tensor* lses, int n, slope_tensor* out,
+                             slope_tensor* lse, void* stream) {
+  if (outs == nullptr || lses == nullptr || out == nullptr) return SLOPE_ERR_NULL;
+  if (n < 1 || n > kMaxMerge) return SLOPE_ERR_SHAPE;
+  if (out->ndim != 3) return SLOPE_ERR_SHAPE;
+  const int64_t S = out->shape[0], H = out->shape[1], dv = out->shape[2];
+  if (dv != 64 && dv != 128) return SLOPE_ERR_UNSUPPORTED;
+  if (S < 0 || S > kMaxSeq || H <= 0 || H > 65535) return SLOPE_ERR_SHAPE;
+  slope_status st;
+  if ((st = check_out(out, S, H, dv, true)) != SLOPE_OK) return st;
+  if (lse != nullptr && (st = check_lse(lse, H, S)) != SLOPE_OK) return st;
+  MergeParams mp{};
+  for (int i = 0; i < n; ++i) {
+    if ((st = check_out(&outs[i], S, H, dv, false)) != SLOPE_OK) return st;
+    if ((st = check_lse(&lses[i], H, S)) != SLOPE_OK) return st;
+    mp.outs[i] = static_cast<const float*>(outs[i].data);
+    mp.o_srow[i] = outs[i].stride[0];
+    mp.o_shead[i] = outs[i].stride[1];
+    mp.lses[i] = static_cast<const float*>(lses[i].data);
+    mp.l_srow[i] = lses[i].stride[1];
+    mp.l_shead[i] = lses[i].stride[0];
+  }
+  if (S == 0) return SLOPE_OK;
+  mp.n = n;
+  mp.H = static_cast<int32_t>(H);
+  mp.dv = static_cast<int32_t>(dv);
+  mp.S = S;
+  mp.out = out->data;
+  mp.out_bf16 = out->dtype == SLOPE_BF16 ? 1 : 0;
+  mp.out_srow = out->stride[0];
+  mp.out_shead = out->stride[1];
+  mp.lse = lse != nullptr ? static_cast<float*>(lse->data) : nullptr;
+  mp.lse_srow = lse != nullptr ? lse->stride[1] : 0;
+  mp.lse_shead = lse != nullptr ? lse->stride[0] : 0;
+  return launch_lse_merge(mp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SLOPE_OK : SLOPE_ERR_CUDA;
+}
+
+size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t dv, int n_chunks, slope_layout layout,
+                                       const int64_t* chunk_sizes) {
+  if (S <= 0 || S > kMaxSeq || Hq <= 0 || (dv != 64 && dv != 128)) return 0;
+  Plan plan;
+  if (build_plan(S, n_chunks, layout, chunk_sizes, 1, 0, plan) != SLOPE_OK) return 0;
+  return workspace_layout(S, Hq, dv, plan.n_planes).total;
+}
+
+slope_status slope_cp_prefill(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
+                              slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
+                              float scale, slope_tensor* out, slope_tensor* lse, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, out, lse, workspace,
+                         workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+slope_status slope_cp_prefill_timed(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v,
+                                    int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
+                                    int64_t window, float scale, slope_tensor* out, slope_tensor* lse,
+                                    void* workspace, size_t workspace_bytes, void* stream, void** events,
+                                    int n_event_pairs, int* n_launches, int* launch_kind) {
+  if (events == nullptr || n_launches == nullptr) return SLOPE_ERR_NULL;
+  Timing tm;
+  tm.events = events;
+  tm.capacity = n_event_pairs;
+  tm.kinds = launch_kind;
+  // count launches first so that a short event array is an argument error, not a partial run
+  if (q != nullptr && q->ndim == 3) {
+    Plan plan;
+    if (build_plan(q->shape[0], n_chunks, layout, chunk_sizes, causal, window, plan) == SLOPE_OK) {
+      int needed = 1;
+      size_t i = 0;
+      for (int l = 0; l < plan.n_launches; ++l) {
+        size_t c = 0;
+        while (i < plan.items.size() && plan.items[i].launch == l) ++i, ++c;
+        needed += static_cast<int>((c + kMaxItems - 1) / kMaxItems);
+      }
+      if (needed > n_event_pairs) return SLOPE_ERR_SHAPE;
+    }
+  }
+  slope_status st = cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, out, lse,
+                                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream), &tm);
+  *n_launches = tm.count;
+  return st;
+}
+
+int64_t slope_cp_prefill_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
+                              int64_t window, slope_plan_item* items, int64_t capacity, int32_t* n_launches,
+                              int32_t* n_planes) {
+  Plan plan;
+  slope_status st = build_plan(S, n_chunks, layout, chunk_sizes, causal, window, plan);
+  if (st != SLOPE_OK) return st;
+  if (capacity > 0 && items == nullptr) return SLOPE_ERR_NULL;
+  for (int64_t i = 0; i < static_cast<int64_t>(plan.items.size()) && i < capacity; ++i) {
+    const PItem& p = plan.items[i];
+    slope_plan_item& o = items[i];
+    std::memset(&o, 0, sizeof(o));
+    o.launch = p.launch;
+    o.plane = p.plane;
+    o.q_row0 = p.q_row0;
+    o.q_len = p.q_len;
+    o.n_kv = p.n_kv;
+    for (int r = 0; r < p.n_kv; ++r) {
+      o.kv_row0[r] = p.kv[r].row0;
+      o.kv_len[r] = p.kv[r].len;
+    }
+  }
+  if (n_launches != nullptr) *n_launches = plan.n_launches;
+  if (n_planes != nullptr) *n_planes = plan.n_planes;
+  return static_cast<int64_t>(plan.items.size());
+}
+
+slope_status slope_device_status(void* stream, int* site) {
+  if (site != nullptr) *site = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SLOPE_ERR_CUDA;
+  int* ptr = device_status_ptr();
+  if (ptr == nullptr) return SLOPE_ERR_CUDA;
+  int word[2] = {0, 0};
+  if (cudaMemcpy(word, ptr, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return SLOPE_ERR_CUDA;
+  if (word[0] == 0) return SLOPE_OK;
+  const int zero[2] = {0, 0};
+  if (cudaMemcpy(ptr, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SLOPE_ERR_CUDA;
+  if (site != nullptr) *site = word[1];
+  return SLOPE_ERR_TIMEOUT;
+}
+
+slope_status slope_debug_timeout_selftest(uint64_t limit_ns, void* stream) {
+  if (limit_ns < 1000ull || limit_ns > 5000000000ull) return SLOPE_ERR_SHAPE;
+  int* ptr = device_status_ptr();
+  if (ptr == nullptr) return SLOPE_ERR_CUDA;
+  return launch_timeout_selftest(limit_ns, ptr, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SLOPE_OK
+                                                                                                   : SLOPE_ERR_CUDA;
+}
+
+const char* slope_status_string(slope_status s) {
+  switch (s) {
+    case SLOPE_OK: return "ok";
+    case SLOPE_ERR_NULL: return "null pointer";
+    case SLOPE_ERR_DTYPE: return "wrong dtype";
+    case SLOPE_ERR_SHAPE: return "bad or inconsistent shape";
+    case SLOPE_ERR_STRIDE: return "bad stride or alignment";
+    case SLOPE_ERR_LAYOUT: return "layout does not divide the sequence";
+    case SLOPE_ERR_CUDA: return "CUDA error";
+    case SLOPE_ERR_TIMEOUT: return "bounded device wait timed out";
+    case SLOPE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SLOPE_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+  }
+  return "unknown status";
+}
+
+const char* slope_version(void) { return "slope-gb300 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

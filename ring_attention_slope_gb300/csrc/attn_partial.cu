@@ -1,0 +1,454 @@
+// Partial attention kernel (one ring step / one chunked-prefill launch).
+//
+// Computes, for every work item (a block of query rows and up to two
+// key/value row ranges), softmax attention restricted to the visible keys of
+// those ranges and writes the normalised output plus its natural-log
+// log-sum-exp: the per-device partial of Ring Attention (Moreh, "Optimizing
+// long-context prefill on multiple older-generation GPU nodes", section
+// "Introduction to Context Parallelism", Ring Attention item), combined later
+// by the log-sum-exp merge.
+//
+// Structure (one CTA = one item x 256 query rows x one query head):
+//   warp 0      TMA producer: Q tiles once, then K and V tiles through a ring
+//               of shared-memory slots (128-byte swizzle, 64-column chunks).
+//   warp 1      MMA issuer: S_t = Q_t K^T (SS, K-major) into TMEM, then
+//               O_t += P_t V (P from TMEM, V MN-major) for the two Q tiles.
+//   warp 2      owns the 512-column TMEM allocation.
+//   warps 4-7   online softmax of Q tile 0 (one query row per thread = TMEM lane),
+//   warps 8-11  online softmax of Q tile 1; each also runs its tile's epilogue.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+dv), O_1 after it.
+// P_t (bf16 pairs) overwrites the first 64 columns of S_t after S_t is read.
+// Scores live in the log2 domain (scale * log2 e folded into one FMA); the
+// running max is only moved when it grows by more than 8 (factor 256), which
+// keeps every p <= 256 and makes most O rescales unnecessary; the final
+// normalisation uses the same max, so the result is exact either way.
+#include "kernels.cuh"
+#include "sm103_ptx.cuh"
+#include "waits.cuh"
+
+namespace slope {
+namespace {
+
+constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 64 bf16 (128 bytes)
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;    // log2 units
+
+template <int DQK, int DV>
+struct K1Cfg {
+  static_assert(DQK % 64 == 0 && DV % 64 == 0, "head dims are multiples of 64");
+  static constexpr int kQChunks = DQK / 64;
+  static constexpr int kVChunks = DV / 64;
+  static constexpr int kQTileBytes = kQChunks * kChunkBytes;
+  static constexpr int kKTileBytes = kQChunks * kChunkBytes;
+  static constexpr int kVTileBytes = kVChunks * kChunkBytes;
+  static constexpr int kSlotBytes = kKTileBytes > kVTileBytes ? kKTileBytes : kVTileBytes;
+  static constexpr int kSlots = DQK == 64 ? 8 : (DQK == 128 ? 4 : 2);
+  static constexpr int kNumBars = 1 + 2 * kSlots + 3 * kQTiles + 1;
+  static constexpr int kBarOffset = kQTiles * kQTileBytes + kSlots * kSlotBytes;
+  static constexpr int kSmemBytes = 1024 + kBarOffset + 8 * kNumBars + 16;
+  static constexpr uint32_t kColO = 256;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kColO + kQTiles * DV <= 512, "TMEM budget");
+};
+
+__device__ __forceinline__ int floor_div(int a, int b) {
+  int q = a / b;
+  if ((a % b) != 0 && (a < 0)) --q;
+  return q;
+}
+
+struct TileGeom {
+  int rows[kQTiles];  // valid query rows of each tile (0 = tile unused)
+  int qa[kQTiles];    // global position of the tile's first row
+  int qb[kQTiles];    // global position of its last valid row
+};
+
+struct Step {
+  int krow;       // first key row of the K/V tile
+  int kpos;       // its global position
+  int valid;      // keys of the range inside the tile (<= 128)
+  uint32_t part;  // bit t: Q tile t sees at least one key of the tile
+  uint32_t full;  // bit t: Q tile t sees every key of the tile (no masking)
+};
+
+// Enumerates the K/V tiles of an item that at least one Q tile of this CTA can
+// see, in the same order for every role.  f returns false to stop (abort).
+template <typename F>
+__device__ __forceinline__ bool for_each_step(const WorkItem& it, const AttnParams& p, const TileGeom& g, F&& f) {
+  const int qa_min = g.qa[0];
+  const int qb_max = g.rows[1] > 0 ? g.qb[1] : g.qb[0];
+  for (int r = 0; r < it.n_kv; ++r) {
+    const int row0 = it.kv[r].row0, len = it.kv[r].len;
+    const int kpos0 = p.kv_pos_off + row0;
+    int lo = 0, hi = (len + kBlockN - 1) / kBlockN - 1;
+    if (p.causal) hi = min(hi, floor_div(qb_max - kpos0, kBlockN));
+    if (p.window > 0) lo = max(lo, floor_div(qa_min - p.window + 1 - kpos0, kBlockN));
+    for (int j = lo; j <= hi; ++j) {
+      Step s;
+      s.krow = row0 + j * kBlockN;
+      s.kpos = kpos0 + j * kBlockN;
+      s.valid = min(kBlockN, len - j * kBlockN);
+      const int klast = s.kpos + s.valid - 1;
+      s.part = 0;
+      s.full = 0;
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t) {
+        if (g.rows[t] <= 0) continue;
+        const bool vis = (!p.causal || s.kpos <= g.qb[t]) && (p.window == 0 || g.qa[t] - klast < p.window);
+        if (!vis) continue;
+        s.part |= 1u << t;
+        const bool full = s.valid == kBlockN && (!p.causal || klast <= g.qa[t]) &&
+                          (p.window == 0 || g.qb[t] - s.kpos < p.window);
+        if (full) s.full |= 1u << t;
+      }
+      if (s.part && !f(s)) return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(kK1Threads, 1)
+    attn_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
+  using C = K1Cfg<DQK, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sSlot = smem + kQTiles * C::kQTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+  uint64_t* bar_q = bars;
+  uint64_t* bar_full = bars + 1;
+  uint64_t* bar_empty = bar_full + C::kSlots;
+  uint64_t* bar_s = bar_empty + C::kSlots;
+  uint64_t* bar_p = bar_s + kQTiles;
+  uint64_t* bar_o = bar_p + kQTiles;
+  uint64_t* bar_drain = bar_o + kQTiles;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + 1);
+  volatile int* cta_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- which item / row block / head this CTA computes
+  const int bid = blockIdx.x;
+  int ii = 0;
+  while (ii < p.n_items - 1 && bid >= (p.items[ii].cta_begin + p.items[ii].n_blocks) * p.Hq) ++ii;
+  const WorkItem itm = p.items[ii];
+  const int local = bid - itm.cta_begin * p.Hq;
+  const int blk = itm.n_blocks - 1 - local / p.Hq;  // heavier (later) row blocks first
+  const int h = local % p.Hq;
+  const int g = h / p.group;
+  TileGeom geo;
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    geo.rows[t] = max(0, min(kBlockM, itm.q_len - blk * kRowsPerCta - t * kBlockM));
+    geo.qa[t] = p.q_pos_off + itm.q_row0 + blk * kRowsPerCta + t * kBlockM;
+    geo.qb[t] = geo.qa[t] + geo.rows[t] - 1;
+  }
+
+  // ---- a CTA scheduled after a timeout elsewhere does nothing
+  if (threadIdx.x == 0) *cta_abort = (*reinterpret_cast<volatile int*>(p.status) != 0) ? 1 : 0;
+  __syncthreads();
+  if (*cta_abort) return;
+
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], 4);
+      mbar_init(&bar_o[t], 1);
+    }
+    mbar_init(bar_drain, 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t limit = p.wait_limit_ns;
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      const int nq = geo.rows[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(bar_q, nq * C::kQTileBytes);
+      for (int t = 0; t < nq; ++t)
+        for (int c = 0; c < C::kQChunks; ++c)
+          tma_load_3d(sQ + t * C::kQTileBytes + c * kChunkBytes, &tm_q, bar_q, 64 * c, h,
+                      itm.q_row0 + blk * kRowsPerCta + t * kBlockM);
+      uint32_t cnt = 0;
+      const bool ok = for_each_step(itm, p, geo, [&](const Step& s) -> bool {
+        {  // K tile
+          const uint32_t slot = cnt % C::kSlots, ph = (cnt / C::kSlots) & 1;
+          if (!wait_bounded(&bar_empty[slot], ph ^ 1, cta_abort, p.status, limit, 1)) return false;
+          mbar_arrive_expect_tx(&bar_full[slot], C::kKTileBytes);
+          for (int c = 0; c < C::kQChunks; ++c)
+            tma_load_3d(sSlot + slot * C::kSlotBytes + c * kChunkBytes, &tm_k, &bar_full[slot], 64 * c, g, s.krow);
+          ++cnt;
+        }
+        {  // V tile
+          const uint32_t slot = cnt % C::kSlots, ph = (cnt / C::kSlots) & 1;
+          if (!wait_bounded(&bar_empty[slot], ph ^ 1, cta_abort, p.status, limit, 2)) return false;
+          mbar_arrive_expect_tx(&bar_full[slot], C::kVTileBytes);
+          for (int c = 0; c < C::kVChunks; ++c)
+            tma_load_3d(sSlot + slot * C::kSlotBytes + c * kChunkBytes, &tm_v, &bar_full[slot], 64 * c, g, s.krow);
+          ++cnt;
+        }
+        return true;
+      });
+      if (!ok) {
+        // let the loads already issued land before the CTA gives up its shared memory
+        wait_final(bar_q, 0, limit);
+        for (uint32_t s = 0; s < C::kSlots && s < cnt; ++s) {
+          const uint32_t last = s + ((cnt - 1 - s) / C::kSlots) * C::kSlots;
+          wait_final(&bar_full[s], (last / C::kSlots) & 1, limit);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, DV, 0, 1);
+      uint32_t cnt = 0;
+      int n[kQTiles] = {0, 0};
+      if (wait_bounded(bar_q, 0, cta_abort, p.status, limit, 3)) {
+        tc_fence_after_sync();
+        for_each_step(itm, p, geo, [&](const Step& s) -> bool {
+          const uint32_t kslot = cnt % C::kSlots, kph = (cnt / C::kSlots) & 1;
+          ++cnt;
+          if (!wait_bounded(&bar_full[kslot], kph, cta_abort, p.status, limit, 4)) return false;
+          tc_fence_after_sync();
+          const uint32_t kbase = smem_u32(sSlot + kslot * C::kSlotBytes);
+#pragma unroll
+          for (int t = 0; t < kQTiles; ++t) {
+            if (!((s.part >> t) & 1)) continue;
+            if (n[t] > 0) {  // S_t/P_t are free once the previous PV of tile t is done
+              if (!wait_bounded(&bar_o[t], (n[t] - 1) & 1, cta_abort, p.status, limit, 5)) return false;
+              tc_fence_after_sync();
+            }
+            const uint32_t qbase = smem_u32(sQ + t * C::kQTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < DQK / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+              mma_ss(tmem + t * kBlockN, smem_desc(qbase + off, 16, 1024, kSwizzle128B),
+                     smem_desc(kbase + off, 16, 1024, kSwizzle128B), idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bar_s[t]);
+          }
+          mma_commit(&bar_empty[kslot]);
+
+          const uint32_t vslot = cnt % C::kSlots, vph = (cnt / C::kSlots) & 1;
+          ++cnt;
+          if (!wait_bounded(&bar_full[vslot], vph, cta_abort, p.status, limit, 6)) return false;
+          tc_fence_after_sync();
+          const uint32_t vbase = smem_u32(sSlot + vslot * C::kSlotBytes);
+#pragma unroll
+          for (int t = 0; t < kQTiles; ++t) {
+            if (!((s.part >> t) & 1)) continue;
+            if (!wait_bounded(&bar_p[t], n[t] & 1, cta_abort, p.status, limit, 7)) return false;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < kBlockN / 16; ++kk) {
+              mma_ts(tmem + C::kColO + t * DV, tmem + t * kBlockN + kk * 8,
+                     smem_desc(vbase + kk * 2048, kChunkBytes, 1024, kSwizzle128B), idesc_pv,
+                     (n[t] > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&bar_o[t]);
+            ++n[t];
+          }
+          mma_commit(&bar_empty[vslot]);
+          return true;
+        });
+      }
+      // every MMA (and the arrivals its commits make) completes before teardown
+      mma_commit(bar_drain);
+      wait_final(bar_drain, 0, limit);
+    }
+  } else if (warp >= 4) {
+    // ================================================================ softmax + epilogue
+    const int t = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * kBlockN;
+    const uint32_t tO = tmem + lane_base + C::kColO + t * DV;
+    const int q_pos = geo.qa[t] + row;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY;  // running max in log2-scaled units
+    float l = 0.f;             // running sum of exp2(s*sl2 - m_used)
+    int n = 0;
+    bool ok = true;
+    if (geo.rows[t] > 0) {
+      ok = for_each_step(itm, p, geo, [&](const Step& s) -> bool {
+        if (!((s.part >> t) & 1)) return true;
+        if (!warp_all(wait_bounded(&bar_s[t], n & 1, cta_abort, p.status, limit, 8))) return false;
+        tc_fence_after_sync();
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(tS + 0, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
+        tmem_ld_wait();
+        reg_fence(r0);
+        reg_fence(r1);
+        reg_fence(r2);
+        reg_fence(r3);
+        float sv[128];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          sv[i] = __uint_as_float(r0[i]);
+          sv[32 + i] = __uint_as_float(r1[i]);
+          sv[64 + i] = __uint_as_float(r2[i]);
+          sv[96 + i] = __uint_as_float(r3[i]);
+        }
+        if (!((s.full >> t) & 1)) {
+#pragma unroll
+          for (int c = 0; c < kBlockN; ++c) {
+            const int kp = s.kpos + c;
+            const bool vis = c < s.valid && (!p.causal || kp <= q_pos) && (p.window == 0 || q_pos - kp < p.window);
+            if (!vis) sv[c] = -INFINITY;
+          }
+        }
+        float mx = sv[0];
+#pragma unroll
+        for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, sv[c]);
+        const float m_new = mx * sl2;
+        const bool need = m_new > m_used + kRescaleThreshold;
+        const bool any_need = __any_sync(0xffffffffu, need);
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m_used - m_new);
+          m_used = m_new;
+          l *= alpha;
+        }
+        const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2_approx(fmaf(sv[32 * c + 2 * i], sl2, -msub));
+            const float p1 = ex2_approx(fmaf(sv[32 * c + 2 * i + 1], sl2, -msub));
+            l += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + c * 16, pk);
+        }
+        tmem_st_wait();
+        if (any_need && n > 0) {  // rescale O_t once the previous PV into it has finished
+          if (!warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 9))) return false;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+            reg_fence(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + c * 32, o);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_p[t]);
+        ++n;
+        return true;
+      });
+
+      // ---- epilogue: out = O / l, lse = ln(sum exp(scaled scores))
+      if (ok && n > 0) ok = warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 10));
+      if (ok) {
+        const bool valid_row = row < geo.rows[t];
+        const int64_t orow = static_cast<int64_t>(itm.out_row0) + blk * kRowsPerCta + t * kBlockM + row;
+        float* op = p.out + static_cast<int64_t>(itm.plane) * p.out_splane + orow * p.out_srow +
+                    static_cast<int64_t>(h) * p.out_shead;
+        if (n > 0) {
+          tc_fence_after_sync();
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+            reg_fence(o);
+            if (valid_row) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                       __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+                *reinterpret_cast<float4*>(op + c * 32 + 4 * i) = v;
+              }
+            }
+          }
+        } else if (p.write_empty_out && valid_row) {
+#pragma unroll
+          for (int i = 0; i < DV / 4; ++i) *reinterpret_cast<float4*>(op + 4 * i) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (valid_row) {
+          p.lse[static_cast<int64_t>(itm.plane) * p.lse_splane + orow * p.lse_srow +
+                static_cast<int64_t>(h) * p.lse_shead] = l > 0.f ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DQK, int DV>
+cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                        cudaStream_t stream) {
+  using C = K1Cfg<DQK, DV>;
+  if (p.n_items <= 0) return cudaSuccess;
+  const WorkItem& last = p.items[p.n_items - 1];
+  const long long ctas = static_cast<long long>(last.cta_begin + last.n_blocks) * p.Hq;
+  if (ctas <= 0) return cudaSuccess;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  attn_partial_kernel<DQK, DV><<<static_cast<unsigned>(ctas), kK1Threads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attn_partial_supported(int dqk, int dv) {
+  return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 64) || (dqk == 128 && dv == 128) ||
+         (dqk == 192 && dv == 128);
+}
+
+cudaError_t launch_attn_partial(int dqk, int dv, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const AttnParams& p, cudaStream_t stream) {
+  if (dqk == 64 && dv == 64) return launch_impl<64, 64>(tq, tk, tv, p, stream);
+  if (dqk == 128 && dv == 64) return launch_impl<128, 64>(tq, tk, tv, p, stream);
+  if (dqk == 128 && dv == 128) return launch_impl<128, 128>(tq, tk, tv, p, stream);
+  if (dqk == 192 && dv == 128) return launch_impl<192, 128>(tq, tk, tv, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace slope

@@ -1,0 +1,88 @@
+// Parameter blocks shared by the host launcher and the two kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace slope {
+
+// ---------------------------------------------------------------- attention partial (K1)
+
+constexpr int kBlockM = 128;      // query rows per Q tile (= TMEM lanes)
+constexpr int kBlockN = 128;      // keys per K/V tile
+constexpr int kQTiles = 2;        // Q tiles per CTA; they share every K/V tile
+constexpr int kRowsPerCta = kBlockM * kQTiles;
+constexpr int kK1Threads = 384;   // warp 0 TMA, warp 1 MMA, warp 2 TMEM owner, 4..11 softmax
+constexpr int kMaxItems = 32;     // work items per launch
+constexpr int kMaxKvRanges = 2;   // key/value ranges per item
+
+struct KvRange {
+  int32_t row0;  // first key row (in the k/v tensors)
+  int32_t len;   // keys in the range
+};
+
+// One query block and the key/value ranges it attends to in this launch.
+struct WorkItem {
+  int32_t q_row0;     // first query row (in q)
+  int32_t q_len;      // query rows
+  int32_t out_row0;   // output row of q_row0
+  int32_t plane;      // output plane
+  int32_t n_kv;       // 0..kMaxKvRanges
+  int32_t cta_begin;  // first CTA-row-block of this item (prefix sum over items)
+  int32_t n_blocks;   // ceil(q_len / kRowsPerCta)
+  KvRange kv[kMaxKvRanges];
+};
+
+struct AttnParams {
+  int32_t n_items;
+  int32_t Hq;
+  int32_t group;            // Hq / Hkv
+  int32_t causal;
+  int32_t window;           // 0 = none
+  int32_t q_pos_off;        // global position of q row 0
+  int32_t kv_pos_off;       // global position of k row 0
+  int32_t write_empty_out;  // write zeros to out for rows that see no key
+  float scale_log2;         // softmax scale * log2(e)
+  float* out;               // fp32 partial output planes
+  int64_t out_srow, out_shead, out_splane;
+  float* lse;               // fp32 log-sum-exp planes
+  int64_t lse_srow, lse_shead, lse_splane;
+  int* status;              // device status word {code, site}
+  uint64_t wait_limit_ns;   // bound on every barrier wait
+  WorkItem items[kMaxItems];
+};
+
+// ---------------------------------------------------------------- merge (K2)
+
+constexpr int kMaxMerge = 32;
+constexpr int kMergeThreads = 256;
+
+struct MergeParams {
+  int32_t n;
+  int32_t H;
+  int32_t dv;
+  int32_t out_bf16;
+  int64_t S;
+  const float* outs[kMaxMerge];
+  const float* lses[kMaxMerge];
+  int64_t o_srow[kMaxMerge], o_shead[kMaxMerge];
+  int64_t l_srow[kMaxMerge], l_shead[kMaxMerge];
+  void* out;
+  int64_t out_srow, out_shead;
+  float* lse;  // may be null
+  int64_t lse_srow, lse_shead;
+};
+
+// Status codes written into the device status word.
+constexpr int kStatusTimeout = 1;
+
+// Host-side launchers (defined in attn_partial.cu / lse_merge.cu / status.cu).
+cudaError_t launch_attn_partial(int dqk, int dv, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const AttnParams& p, cudaStream_t stream);
+bool attn_partial_supported(int dqk, int dv);
+cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_timeout_selftest(uint64_t limit_ns, int* status, cudaStream_t stream);
+int* device_status_ptr();  // per current device; nullptr on failure
+
+}  // namespace slope

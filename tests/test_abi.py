@@ -1,0 +1,119 @@
+"""The C ABI library loads without a GPU and exports every declared symbol;
+argument errors are reported as statuses before anything touches the GPU."""
+import ctypes
+
+import pytest
+
+import ring_attention_slope_gb300 as slope
+from _lib import built_lib, declared_symbols
+
+S_OK, E_NULL, E_DTYPE, E_SHAPE, E_STRIDE, E_LAYOUT, E_CUDA, E_TIMEOUT, E_UNSUP, E_WS = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return built_lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert len(names) == 10, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in slope.h but not exported"
+    assert sorted(names) == sorted(slope.EXPORTED)
+
+
+def test_status_strings_and_version(lib):
+    for code in (S_OK, E_NULL, E_DTYPE, E_SHAPE, E_STRIDE, E_LAYOUT, E_CUDA, E_TIMEOUT, E_UNSUP, E_WS):
+        assert slope.status_string(code) not in ("", "unknown status")
+    assert slope.status_string(12345) == "unknown status"
+    assert "sm_103a" in slope.version()
+
+
+def _t(shape, dtype=0, data=0x10000, stride=None):
+    """Descriptor with a fake (never dereferenced) device address."""
+    d = slope.SlopeTensor()
+    d.data = data
+    d.dtype = dtype
+    d.ndim = len(shape)
+    if stride is None:
+        stride = []
+        acc = 1
+        for s in reversed(shape):
+            stride.insert(0, acc)
+            acc *= s
+    for i, s in enumerate(shape):
+        d.shape[i] = s
+        d.stride[i] = stride[i]
+    return d
+
+
+def _cp(lib, q, k, v, out, lse=None, n=4, layout=1, sizes=None, ws=0x20000, ws_bytes=1 << 40, window=0):
+    arr = None
+    if sizes is not None:
+        arr = (ctypes.c_int64 * len(sizes))(*sizes)
+    return lib.slope_cp_prefill(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), n, layout,
+                                ctypes.cast(arr, ctypes.POINTER(ctypes.c_int64)) if arr else None, 1, window, 0.0,
+                                ctypes.byref(out), ctypes.byref(lse) if lse else None, ws, ws_bytes, None)
+
+
+def test_cp_prefill_argument_errors(lib):
+    S, Hq, Hkv, d = 1024, 4, 1, 64
+    q, k, v = _t([S, Hq, d]), _t([S, Hkv, d]), _t([S, Hkv, d])
+    out, lse = _t([S, Hq, d]), _t([Hq, S], dtype=1)
+    assert lib.slope_cp_prefill(None, ctypes.byref(k), ctypes.byref(v), 4, 1, None, 1, 0, 0.0,
+                                ctypes.byref(out), None, 0x20000, 1 << 40, None) == E_NULL
+    assert _cp(lib, q, k, v, out, lse, ws=0) == E_WS                                  # no workspace
+    assert _cp(lib, q, k, v, out, lse, ws_bytes=16) == E_WS                           # too small
+    assert _cp(lib, q, k, v, out, lse, ws=0x20010) == E_WS                            # misaligned
+    assert _cp(lib, _t([S, Hq, d], dtype=1), k, v, out, lse) == E_DTYPE               # fp32 q
+    assert _cp(lib, q, _t([S, 3, d]), _t([S, 3, d]), out, lse) == E_SHAPE            # Hq % Hkv
+    assert _cp(lib, q, k, v, out, lse, n=5) == E_LAYOUT                               # 1024 % 10
+    assert _cp(lib, q, k, v, out, lse, n=3, layout=0) == E_LAYOUT                     # 1024 % 3
+    assert _cp(lib, q, k, v, out, lse, n=2, layout=2, sizes=[500, 500]) == E_LAYOUT   # sizes != S
+    assert _cp(lib, q, k, v, out, lse, n=2, layout=2, sizes=[1024, 0]) == E_LAYOUT    # empty chunk
+    assert _cp(lib, q, k, v, out, lse, n=4, layout=7) == E_LAYOUT                     # unknown layout
+    assert _cp(lib, q, k, v, out, lse, n=0) == E_LAYOUT
+    assert _cp(lib, q, k, v, out, lse, n=33) == E_LAYOUT                              # > 32 ranks
+    assert _cp(lib, _t([S, Hq, 96]), _t([S, Hkv, 96]), _t([S, Hkv, 96]), _t([S, Hq, 96]), lse) == E_UNSUP
+    assert _cp(lib, _t([S, Hq, d], stride=[Hq * d, d, 2]), k, v, out, lse) == E_STRIDE  # inner stride
+    assert _cp(lib, _t([S, Hq, d], stride=[Hq * d + 4, d, 1]), k, v, out, lse) == E_STRIDE  # 8-B row stride
+    assert _cp(lib, _t([S, Hq, d], data=0x10008), k, v, out, lse) == E_STRIDE      # 8-byte aligned base
+    assert _cp(lib, q, k, v, _t([S, Hq, 32]), lse) == E_SHAPE                         # out dv
+    assert _cp(lib, q, k, v, out, _t([S, Hq], dtype=1)) == E_SHAPE                    # lse transposed
+    assert _cp(lib, q, k, v, out, lse, window=-1) == E_SHAPE
+
+
+def test_attn_partial_and_merge_argument_errors(lib):
+    Sq, Skv, Hq, Hkv, d = 300, 200, 8, 2, 128
+    q, k, v = _t([Sq, Hq, d]), _t([Skv, Hkv, d]), _t([Skv, Hkv, 64])
+    out, lse = _t([Sq, Hq, 64], dtype=1), _t([Hq, Sq], dtype=1)
+
+    def call(q=q, k=k, v=v, out=out, lse=lse):
+        return lib.slope_attn_partial(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 0, 0, 1, 0, 0.0,
+                                      ctypes.byref(out) if out else None, ctypes.byref(lse) if lse else None, None)
+
+    assert call(out=_t([Sq, Hq, 64], dtype=0)) == E_DTYPE      # partial out must be fp32
+    assert call(lse=None) == E_NULL
+    assert call(v=_t([Skv, Hkv, 192])) == E_UNSUP              # (128, 192)
+    assert call(k=_t([Skv + 1, Hkv, d])) == E_SHAPE
+    assert call(out=_t([Sq, Hq, 64], dtype=1, stride=[Hq * 64, 66, 1])) == E_STRIDE
+    o = (slope.SlopeTensor * 2)(_t([Sq, Hq, 64], dtype=1), _t([Sq, Hq, 64], dtype=1))
+    l = (slope.SlopeTensor * 2)(_t([Hq, Sq], dtype=1), _t([Hq, Sq], dtype=1))
+    fin = _t([Sq, Hq, 64], dtype=0)
+    assert lib.slope_lse_merge(o, l, 0, ctypes.byref(fin), None, None) == E_SHAPE
+    assert lib.slope_lse_merge(o, l, 33, ctypes.byref(fin), None, None) == E_SHAPE
+    l_bad = (slope.SlopeTensor * 2)(_t([Hq, Sq], dtype=1), _t([Hq, Sq + 1], dtype=1))
+    assert lib.slope_lse_merge(o, l_bad, 2, ctypes.byref(fin), None, None) == E_SHAPE
+    o_bad = (slope.SlopeTensor * 2)(_t([Sq, Hq, 64], dtype=1), _t([Sq, Hq, 64], dtype=0))
+    assert lib.slope_lse_merge(o_bad, l, 2, ctypes.byref(fin), None, None) == E_DTYPE
+
+
+def test_workspace_size(lib):
+    # ring: N planes of fp32 [S, Hq, dv] + lse; chunked: 2 planes
+    ws = slope.cp_prefill_workspace_size(1024, 4, 64, 4, "zigzag")
+    assert ws >= 4 * 1024 * 4 * 65 * 4
+    wc = slope.cp_prefill_workspace_size(65536, 64, 64, 6, "chunked", [12288] * 5 + [4096])
+    assert wc >= 2 * 65536 * 64 * 65 * 4
+    assert slope.cp_prefill_workspace_size(1000, 4, 64, 8, "zigzag") == 0
+    assert slope.cp_prefill_workspace_size(1024, 4, 96, 4, "zigzag") == 0

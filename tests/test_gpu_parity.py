@@ -1,0 +1,259 @@
+"""CUDA path (through the C ABI) against the fp64 oracle, element by element.
+
+Tolerances (bf16 inputs, fp32 accumulation): output max-abs <= 2e-2 and
+relative L2 <= 5e-3, log-sum-exp max-abs <= 1e-3; rows that see no key must
+give exactly out = 0 and lse = -inf on both sides.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ring_attention_slope_gb300 as slope
+import slope_workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+OUT_MAX, OUT_REL_L2, LSE_MAX = 2e-2, 5e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    slope.build()
+    slope.load()
+    st, _ = slope.device_status()
+    assert st == 0
+
+
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, what):
+    og = np.asarray(out_gpu, dtype=np.float64)
+    lg = np.asarray(lse_gpu, dtype=np.float64)
+    assert og.shape == out_ref.shape, f"{what}: out shape {og.shape} vs {out_ref.shape}"
+    assert lg.shape == lse_ref.shape, f"{what}: lse shape {lg.shape} vs {lse_ref.shape}"
+    assert np.all(np.isfinite(og)), f"{what}: non-finite output"
+    empty = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lg), empty), f"{what}: -inf rows differ"
+    assert not np.any(np.isnan(lg)), f"{what}: NaN lse"
+    fin = ~empty
+    if fin.any():
+        le = np.max(np.abs(lg[fin] - lse_ref[fin]))
+        assert le <= LSE_MAX, f"{what}: lse max-abs {le:.3e}"
+    d = og - out_ref
+    me = np.max(np.abs(d)) if d.size else 0.0
+    nr = np.linalg.norm(out_ref)
+    rel = np.linalg.norm(d) / nr if nr > 0 else np.linalg.norm(d)
+    assert me <= OUT_MAX, f"{what}: out max-abs {me:.3e}"
+    assert rel <= OUT_REL_L2, f"{what}: out rel-L2 {rel:.3e}"
+    # empty rows: exactly zero output
+    emp_rows = empty.T  # [rows, heads]
+    if emp_rows.any():
+        assert np.all(og[emp_rows] == 0.0), f"{what}: nonzero output for rows with no visible key"
+    return me, rel
+
+
+def qkv(S, Hq, Hkv, dqk, dv, seed, Skv=None, scale_v=1.0, device="cuda"):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    Skv = S if Skv is None else Skv
+    q = (torch.randn(S, Hq, dqk, generator=g) * scale_v).to(torch.bfloat16)
+    k = (torch.randn(Skv, Hkv, dqk, generator=g) * scale_v).to(torch.bfloat16)
+    v = (torch.randn(Skv, Hkv, dv, generator=g) * scale_v).to(torch.bfloat16)
+    return q.to(device), k.to(device), v.to(device)
+
+
+# ---------------------------------------------------------------- device status / bounded waits
+
+def test_timeout_selftest_reports_and_context_survives():
+    slope.timeout_selftest(2_000_000)  # 2 ms limit on a barrier nothing completes
+    st, site = slope.device_status()
+    assert st == -7 and site == 99
+    assert slope.device_status() == (0, 0)  # cleared by the read
+    q, k, v = qkv(256, 2, 1, 64, 64, seed=1)
+    out, lse = slope.attn_partial(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True)
+    compare(out.cpu(), lse.cpu(), ro, rl, "after timeout self-test")
+    assert slope.device_status() == (0, 0)
+
+
+# ---------------------------------------------------------------- partial attention
+
+PARTIAL_CASES = [
+    # Sq, Skv, Hq, Hkv, dqk, dv, q_off, kv_off, causal, window
+    (256, 256, 2, 1, 64, 64, 0, 0, True, 0),
+    (300, 300, 4, 2, 64, 64, 0, 0, True, 0),          # ragged query tail, several tiles
+    (517, 700, 4, 1, 64, 64, 183, 0, True, 0),        # queries after a longer key prefix
+    (384, 384, 8, 8, 64, 64, 1000, 0, False, 0),      # unmasked
+    (260, 390, 4, 2, 64, 64, 390, 0, True, 0),        # keys all earlier: full tiles + ragged key tail
+    (200, 333, 2, 1, 64, 64, 0, 100, True, 0),        # keys partly in the future; first rows see none
+    (640, 640, 2, 1, 64, 64, 0, 0, True, 128),        # sliding window 128
+    (500, 500, 2, 2, 64, 64, 0, 0, True, 1),          # window 1: out = v
+    (333, 333, 4, 1, 64, 64, 0, 0, True, 77),
+    (256, 256, 4, 2, 128, 64, 0, 0, True, 0),
+    (300, 410, 2, 1, 128, 128, 110, 0, True, 0),
+    (384, 384, 2, 2, 192, 128, 0, 0, True, 0),        # MLA-shaped
+    (270, 513, 3, 3, 192, 128, 243, 0, True, 0),
+    (1, 1, 1, 1, 64, 64, 0, 0, True, 0),
+    (129, 1, 2, 1, 64, 64, 5, 4, True, 0),
+]
+
+
+@pytest.mark.parametrize("case", PARTIAL_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_attn_partial_matches_oracle(case):
+    Sq, Skv, Hq, Hkv, dqk, dv, q_off, kv_off, causal, window = case
+    q, k, v = qkv(Sq, Hq, Hkv, dqk, dv, seed=hash(case) % 10000, Skv=Skv, scale_v=1.0)
+    out, lse = slope.attn_partial(q, k, v, q_off=q_off, kv_off=kv_off, causal=causal, window=window)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), q_pos0=q_off, kv_pos0=kv_off, causal=causal,
+                              window=window)
+    compare(out.cpu(), lse.cpu(), ro, rl, f"partial {case}")
+    assert slope.device_status() == (0, 0)
+
+
+def test_attn_partial_no_keys_and_future_keys():
+    q, k, v = qkv(200, 4, 2, 64, 64, seed=5, Skv=300)
+    out, lse = slope.attn_partial(q, k, v, q_off=0, kv_off=500, causal=True)  # every key in the future
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+    out, lse = slope.attn_partial(q, k[:0], v[:0], causal=True)  # no keys at all
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_attn_partial_window1_is_exact_identity():
+    q, k, v = qkv(300, 2, 1, 64, 64, seed=6)
+    out, lse = slope.attn_partial(q, k, v, causal=True, window=1)
+    torch.cuda.synchronize()
+    G = 2
+    ref = v.float().repeat_interleave(G, dim=1)
+    torch.testing.assert_close(out, ref, rtol=1e-6, atol=0)
+    sii = (q.float() * k.float().repeat_interleave(G, dim=1)).sum(-1) / 8.0  # scale 1/sqrt(64)
+    torch.testing.assert_close(lse, sii.T.contiguous(), rtol=0, atol=1e-5)
+
+
+def test_attn_partial_strided_views():
+    """Q/K/V as head-slices of larger packed tensors; out/lse as views with padding."""
+    S, Hq, Hkv, d = 300, 4, 2, 64
+    g = torch.Generator().manual_seed(11)
+    qkv_packed = torch.randn(S, Hq + 2 * Hkv, d, generator=g).to(torch.bfloat16).cuda()
+    q, k, v = qkv_packed[:, :Hq], qkv_packed[:, Hq:Hq + Hkv], qkv_packed[:, Hq + Hkv:]
+    out_big = torch.full((S, Hq + 1, d), 7.0, device="cuda")
+    lse_big = torch.full((Hq, S + 16), 7.0, device="cuda")
+    out, lse = slope.attn_partial(q, k, v, causal=True, out=out_big[:, :Hq], lse=lse_big[:, :S])
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True)
+    compare(out.cpu(), lse.cpu(), ro, rl, "strided views")
+    assert torch.all(out_big[:, Hq] == 7.0) and torch.all(lse_big[:, S:] == 7.0)
+
+
+# ---------------------------------------------------------------- merge
+
+@pytest.mark.parametrize("dv", [64, 128])
+@pytest.mark.parametrize("n", [1, 2, 5, 16, 32])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_lse_merge_matches_oracle(dv, n, out_dtype):
+    S, H = 333, 6
+    g = torch.Generator().manual_seed(n * 100 + dv)
+    outs = [torch.randn(S, H, dv, generator=g) for _ in range(n)]
+    lses = [torch.randn(H, S, generator=g) * 4 + 2 for _ in range(n)]
+    for i, l in enumerate(lses):  # some partials see nothing for some rows
+        l[:, (torch.arange(S) % (i + 2)) == 0] = -math.inf
+    lses[0][:, :5] = -math.inf
+    for l in lses:
+        l[:, :3] = -math.inf  # rows 0..2 see nothing at all
+    out, lse = slope.lse_merge([o.cuda() for o in outs], [x.cuda() for x in lses], out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    ro, rl = oracle.merge([o.double().numpy() for o in outs], [x.double().numpy() for x in lses])
+    compare(out.float().cpu(), lse.cpu(), ro, rl, f"merge n={n} dv={dv} {out_dtype}")
+
+
+# ---------------------------------------------------------------- whole prefill: tiny workload, all layouts
+
+def tiny():
+    return wl.WORKLOADS[0]
+
+
+@pytest.mark.parametrize("layout,n", [("zigzag", 4), ("zigzag", 2), ("zigzag", 1), ("contiguous", 4),
+                                      ("contiguous", 8), ("chunked", 3), ("chunked", 1)])
+@pytest.mark.parametrize("window", [0, 128])
+def test_cp_prefill_tiny_all_layouts(layout, n, window):
+    w = tiny()
+    q, k, v = wl.workload_qkv(w, device="cuda")
+    out, lse = slope.cp_prefill(q, k, v, n, layout, window=window)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, window=window)
+    compare(out.float().cpu(), lse.cpu(), ro, rl, f"tiny {layout} n={n} W={window}")
+    assert slope.device_status() == (0, 0)
+
+
+def test_cp_prefill_chunked_ragged_sizes_and_fp32_out():
+    S, Hq, Hkv, d = 1000, 4, 2, 64
+    q, k, v = qkv(S, Hq, Hkv, d, d, seed=21, scale_v=0.8)
+    sizes = [130, 1, 257, 255, 357]
+    out, lse = slope.cp_prefill(q, k, v, len(sizes), "chunked", chunk_sizes=sizes, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True)
+    compare(out.cpu(), lse.cpu(), ro, rl, "chunked ragged")
+
+
+def test_cp_prefill_layout_invariance():
+    """Zigzag, contiguous and chunked decompositions agree with each other."""
+    S, Hq, Hkv, d = 2048, 4, 1, 64
+    q, k, v = qkv(S, Hq, Hkv, d, d, seed=31)
+    res = []
+    for layout, n in (("zigzag", 4), ("contiguous", 8), ("chunked", 5), ("zigzag", 1)):
+        o, l = slope.cp_prefill(q, k, v, n, layout, out_dtype=torch.float32)
+        res.append((o, l))
+    torch.cuda.synchronize()
+    base_o, base_l = res[0][0].cpu().double().numpy(), res[0][1].cpu().double().numpy()
+    for o, l in res[1:]:
+        compare(o.cpu(), l.cpu(), base_o, base_l, "layout invariance")
+
+
+def test_cp_prefill_mla_shape_small():
+    S, H = 1536, 4
+    q, k, v = qkv(S, H, H, 192, 128, seed=41, scale_v=0.3)
+    sizes = [700, 500, 336]
+    out, lse = slope.cp_prefill(q, k, v, 3, "chunked", chunk_sizes=sizes)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True)
+    compare(out.float().cpu(), lse.cpu(), ro, rl, "mla small")
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled rows/heads
+
+def check_full_workload(w, window, rows_random=4096):
+    q, k, v = wl.workload_qkv(w, device="cuda")
+    sizes = wl.chunk_sizes(w)
+    n = wl.n_chunks(w)
+    out, lse = slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window)
+    torch.cuda.synchronize()
+    assert slope.device_status() == (0, 0)
+    rows = wl.sample_rows(w, n_random=rows_random)
+    heads = wl.sample_heads(w)
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    ro, rl = oracle.attention(qc, kc, vc, causal=True, window=window, rows=rows, heads=heads)
+    og = out[torch.from_numpy(rows).cuda()][:, heads].float().cpu()
+    lg = lse[heads][:, torch.from_numpy(rows).cuda()].cpu()
+    compare(og, lg, ro, rl, f"{w.name} W={window}")
+    # properties at every row: finite outputs, lse >= the log of... finite and bounded
+    assert torch.isfinite(out.float()).all()
+    assert torch.isfinite(lse).all()
+
+
+def test_full_causal_gqa_s32k_zigzag8():
+    check_full_workload(wl.WORKLOADS[1], 0)
+
+
+def test_full_chunked_prefill_s64k():
+    check_full_workload(wl.WORKLOADS[2], 0)
+
+
+@pytest.mark.parametrize("window", [0, 128])
+def test_full_s100k_zigzag16(window):
+    check_full_workload(wl.WORKLOADS[3], window, rows_random=2048)
+
+
+def test_full_mla_s64k_chunked_var():
+    check_full_workload(wl.WORKLOADS[4], 0)

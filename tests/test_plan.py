@@ -1,0 +1,112 @@
+"""Host-side work decomposition: ring steps (zigzag / contiguous) and chunked
+prefill items cover every visible (query, key) pair exactly once."""
+import numpy as np
+import pytest
+
+import ring_attention_slope_gb300 as slope
+from _lib import built_lib
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    built_lib()
+
+
+def visible(S, window, causal=True):
+    i = np.arange(S)[:, None]
+    j = np.arange(S)[None, :]
+    m = np.ones((S, S), dtype=bool)
+    if causal:
+        m &= j <= i
+    if window:
+        m &= (i - j) < window
+    return m
+
+
+def coverage(items, S, window, causal=True):
+    vis = visible(S, window, causal)
+    cnt = np.zeros((S, S), dtype=np.int32)
+    for it in items:
+        q0, q1 = it["q_row0"], it["q_row0"] + it["q_len"]
+        for k0, kl in it["kv"]:
+            cnt[q0:q1, k0:k0 + kl] += vis[q0:q1, k0:k0 + kl]
+    return cnt, vis
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("window", [0, 1, 37, 128])
+def test_ring_plan_covers_each_visible_pair_once(layout, N, window):
+    parts = 2 * N if layout == "zigzag" else N
+    S = parts * 24
+    items, n_launches, n_planes = slope.cp_prefill_plan(S, N, layout, window=window)
+    assert n_launches == N and n_planes == N
+    cnt, vis = coverage(items, S, window)
+    assert np.array_equal(cnt, vis.astype(np.int32)), "some visible pair missing or counted twice"
+    # each step is one launch; in it every query row belongs to exactly one item (one partial per row and step)
+    for t in range(N):
+        rows = np.zeros(S, dtype=np.int32)
+        for it in items:
+            if it["launch"] == t:
+                assert it["plane"] == t
+                rows[it["q_row0"]:it["q_row0"] + it["q_len"]] += 1
+        assert np.all(rows == 1)
+    # zigzag ownership: the ranks' query sub-chunks are r and 2N-1-r
+    if layout == "zigzag":
+        sub = S // (2 * N)
+        starts = sorted({it["q_row0"] // sub for it in items if it["launch"] == 0})
+        assert starts == list(range(2 * N))
+
+
+def test_zigzag_balances_causal_work():
+    """Zigzag gives every rank the same causal work; contiguous does not."""
+    S, N = 64 * 16, 8
+    vis = visible(S, 0)
+
+    def per_rank(layout):
+        items, _, _ = slope.cp_prefill_plan(S, N, layout)
+        parts = 2 * N if layout == "zigzag" else N
+        sub = S // parts
+        work = np.zeros(N)
+        for it in items:
+            a = it["q_row0"] // sub
+            r = a if a < N else 2 * N - 1 - a
+            if layout == "contiguous":
+                r = a
+            for k0, kl in it["kv"]:
+                work[r] += vis[it["q_row0"]:it["q_row0"] + it["q_len"], k0:k0 + kl].sum()
+        return work
+
+    zz = per_rank("zigzag")
+    ct = per_rank("contiguous")
+    assert zz.max() / zz.min() < 1.01
+    assert ct.max() / ct.min() > 5
+
+
+@pytest.mark.parametrize("sizes", [[300], [100, 200], [12, 40, 7, 141, 100], None])
+@pytest.mark.parametrize("window", [0, 16])
+def test_chunked_plan(sizes, window):
+    S = 300
+    n = len(sizes) if sizes else 4
+    items, n_launches, n_planes = slope.cp_prefill_plan(S, n, "chunked", chunk_sizes=sizes, window=window)
+    assert n_launches == n and n_planes == 2
+    cnt, vis = coverage(items, S, window)
+    assert np.array_equal(cnt, vis.astype(np.int32))
+    starts = np.cumsum([0] + (sizes or [75] * 4))[:-1]
+    for c in range(n):
+        its = [it for it in items if it["launch"] == c]
+        assert sorted(it["plane"] for it in its) == [0, 1]
+        for it in its:
+            assert it["q_row0"] == starts[c]
+            for k0, kl in it["kv"]:
+                if it["plane"] == 0:
+                    assert k0 + kl <= starts[c]  # prefix partial: earlier tokens only
+                else:
+                    assert k0 >= starts[c]       # own partial: the chunk itself
+
+
+def test_plan_errors():
+    with pytest.raises(slope.SlopeError):
+        slope.cp_prefill_plan(1000, 8, "zigzag")
+    with pytest.raises(slope.SlopeError):
+        slope.cp_prefill_plan(1000, 2, "chunked", chunk_sizes=[400, 500])
