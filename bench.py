@@ -131,6 +131,22 @@ def workload_flops(w, window=0):
     return wl.flops(w, window)
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """Largest value of x over all ranks (the job's time is its slowest rank's)."""
+    import torch
+
+    if dist is None or not dist.is_initialized():
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step: float, steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs its own replica of the step (weak scaling)."""
+    return flops_per_step * steps * world / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- CPU oracle legs
 
 def oracle_sample(w, target_s, seed=0):
@@ -264,11 +280,7 @@ def run_gpu(args, w):
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        tt = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, "cuda")
     st, site = slope.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} at site {site}")
@@ -286,7 +298,7 @@ def run_gpu(args, w):
                 k2_n += 1
 
     flops_step = workload_flops(w, window)
-    value = flops_step * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    value = job_tflops(flops_step, args.steps, world, elapsed_ms)
     tokens_s = w.S * args.steps * world / (elapsed_ms * 1e-3)
     peaks, peak_src = load_peaks()
     k1_tflops = flops_step * args.steps / (k1_ms * 1e-3) / 1e12
@@ -298,7 +310,8 @@ def run_gpu(args, w):
     k2_gbs = merge_bytes * k2_n / (k2_ms * 1e-3) / 1e9 if k2_ms > 0 else None
 
     # ---- end to end through the public call with pinned host buffers
-    e2e = run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier, dist)
+    e2e = None if args.no_e2e else run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier,
+                                           dist)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -379,14 +392,9 @@ def run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrie
         step()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    world = 1
-    if dist is not None:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-        world = dist.get_world_size()
-    val = workload_flops(w, window) * args.steps * world / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(a.elapsed_time(b), dist, "cuda")
+    world = dist.get_world_size() if dist is not None else 1
+    val = job_tflops(workload_flops(w, window), args.steps, world, ms)
     return {"value": val, "unit": UNIT, "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
             "d2h_bytes_per_step": int(ho.numel() * 2 + hl.numel() * 4), "ms_per_step": ms / args.steps}
 
@@ -401,6 +409,7 @@ def main():
     ap.add_argument("--window", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
