@@ -210,6 +210,13 @@ SLOPE_API slope_status slope_device_status(void* stream, int* site);
  */
 SLOPE_API slope_status slope_debug_timeout_selftest(uint64_t limit_ns, void* stream);
 
+/*
+ * Text of the last CUDA runtime/driver failure that made a call of this
+ * library (in the calling thread) return SLOPE_ERR_CUDA, or "" if none.
+ * The pointer stays valid until the next call from the same thread.
+ */
+SLOPE_API const char* slope_last_error(void);
+
 /* Static description of a status code. */
 SLOPE_API const char* slope_status_string(slope_status s);
 

@@ -44,14 +44,17 @@ class SlopePlanItem(ctypes.Structure):
 class SlopeError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {status_string(status)} ({status})")
+        detail = ""
+        if status == -6:
+            detail = " [" + load().slope_last_error().decode() + "]"
+        super().__init__(f"{what}: {status_string(status)} ({status}){detail}")
 
 
 _lib = None
 
 EXPORTED = ["slope_attn_partial", "slope_lse_merge", "slope_cp_prefill", "slope_cp_prefill_workspace_size",
             "slope_cp_prefill_timed", "slope_cp_prefill_plan", "slope_device_status",
-            "slope_debug_timeout_selftest", "slope_status_string", "slope_version"]
+            "slope_debug_timeout_selftest", "slope_status_string", "slope_version", "slope_last_error"]
 
 
 def build(force: bool = False) -> str:
@@ -93,6 +96,8 @@ def load():
     lib.slope_status_string.restype = ctypes.c_char_p
     lib.slope_version.argtypes = []
     lib.slope_version.restype = ctypes.c_char_p
+    lib.slope_last_error.argtypes = []
+    lib.slope_last_error.restype = ctypes.c_char_p
     _lib = lib
     return lib
 

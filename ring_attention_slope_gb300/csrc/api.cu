@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <vector>
@@ -23,6 +24,19 @@ constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s: far beyond any 
 // ---------------------------------------------------------------- argument checks
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+thread_local char g_last_error[256] = "";
+
+// Records the text of a failing CUDA call and returns SLOPE_ERR_CUDA.
+slope_status cuda_fail(const char* where, cudaError_t e) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorString(e),
+                cudaGetErrorName(e));
+  return SLOPE_ERR_CUDA;
+}
+slope_status cuda_fail(const char* where) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s", where);
+  return SLOPE_ERR_CUDA;
+}
 
 // bf16 [S, H, d] readable by TMA: innermost stride 1, other strides multiples of 8 elements.
 slope_status check_qkv(const slope_tensor* t) {
@@ -294,9 +308,11 @@ slope_status run_attention(const std::vector<WorkItem>& group, int dqk, int dv, 
                            cudaStream_t stream) {
   base.n_items = static_cast<int32_t>(group.size());
   for (size_t i = 0; i < group.size(); ++i) base.items[i] = group[i];
-  if (record(tm, true, 0, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
-  if (launch_attn_partial(dqk, dv, tq, tk, tv, base, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
-  if (record(tm, false, 0, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
+  cudaError_t e;
+  if ((e = record(tm, true, 0, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
+  if ((e = launch_attn_partial(dqk, dv, tq, tk, tv, base, stream)) != cudaSuccess)
+    return cuda_fail("attention kernel launch", e);
+  if ((e = record(tm, false, 0, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
   return SLOPE_OK;
 }
 
@@ -335,10 +351,10 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < wl.total) return SLOPE_ERR_WORKSPACE;
   int* status = device_status_ptr();
-  if (status == nullptr) return SLOPE_ERR_CUDA;
+  if (status == nullptr) return cuda_fail("device status word (cudaGetSymbolAddress)");
 
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, q) || !make_map(&tk, k) || !make_map(&tv, v)) return SLOPE_ERR_CUDA;
+  if (!make_map(&tq, q) || !make_map(&tk, k) || !make_map(&tv, v)) return cuda_fail("cuTensorMapEncodeTiled");
 
   float* planes = static_cast<float*>(workspace);
   float* lse_planes = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.lse_offset);
@@ -395,9 +411,10 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   mp.lse = lse != nullptr ? static_cast<float*>(lse->data) : nullptr;
   mp.lse_srow = lse != nullptr ? lse->stride[1] : 0;
   mp.lse_shead = lse != nullptr ? lse->stride[0] : 0;
-  if (record(tm, true, 1, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
-  if (launch_lse_merge(mp, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
-  if (record(tm, false, 1, stream) != cudaSuccess) return SLOPE_ERR_CUDA;
+  cudaError_t e;
+  if ((e = record(tm, true, 1, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
+  if ((e = launch_lse_merge(mp, stream)) != cudaSuccess) return cuda_fail("merge kernel launch", e);
+  if ((e = record(tm, false, 1, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
   return SLOPE_OK;
 }
 
@@ -431,12 +448,12 @@ slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, co
   if ((st = check_lse(lse, Hq, Sq)) != SLOPE_OK) return st;
   if (Sq == 0) return SLOPE_OK;
   int* status = device_status_ptr();
-  if (status == nullptr) return SLOPE_ERR_CUDA;
+  if (status == nullptr) return cuda_fail("device status word (cudaGetSymbolAddress)");
 
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, q)) return SLOPE_ERR_CUDA;
+  if (!make_map(&tq, q)) return cuda_fail("cuTensorMapEncodeTiled");
   if (Skv > 0) {
-    if (!make_map(&tk, k) || !make_map(&tv, v)) return SLOPE_ERR_CUDA;
+    if (!make_map(&tk, k) || !make_map(&tv, v)) return cuda_fail("cuTensorMapEncodeTiled");
   } else {
     tk = tq;  // never read: an item with no key range issues no K/V load
     tv = tq;
@@ -511,7 +528,8 @@ slope_status slope_lse_merge(const slope_tensor* outs, const slope_tensor* lses,
   mp.lse = lse != nullptr ? static_cast<float*>(lse->data) : nullptr;
   mp.lse_srow = lse != nullptr ? lse->stride[1] : 0;
   mp.lse_shead = lse != nullptr ? lse->stride[0] : 0;
-  return launch_lse_merge(mp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SLOPE_OK : SLOPE_ERR_CUDA;
+  const cudaError_t e = launch_lse_merge(mp, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SLOPE_OK : cuda_fail("merge kernel launch", e);
 }
 
 size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t dv, int n_chunks, slope_layout layout,
@@ -588,14 +606,18 @@ int64_t slope_cp_prefill_plan(int64_t S, int n_chunks, slope_layout layout, cons
 
 slope_status slope_device_status(void* stream, int* site) {
   if (site != nullptr) *site = 0;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SLOPE_ERR_CUDA;
+  cudaError_t e;
+  if ((e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return cuda_fail("cudaStreamSynchronize", e);
   int* ptr = device_status_ptr();
-  if (ptr == nullptr) return SLOPE_ERR_CUDA;
+  if (ptr == nullptr) return cuda_fail("device status word (cudaGetSymbolAddress)");
   int word[2] = {0, 0};
-  if (cudaMemcpy(word, ptr, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return SLOPE_ERR_CUDA;
+  if ((e = cudaMemcpy(word, ptr, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail("cudaMemcpy", e);
   if (word[0] == 0) return SLOPE_OK;
   const int zero[2] = {0, 0};
-  if (cudaMemcpy(ptr, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SLOPE_ERR_CUDA;
+  if ((e = cudaMemcpy(ptr, zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail("cudaMemcpy", e);
   if (site != nullptr) *site = word[1];
   return SLOPE_ERR_TIMEOUT;
 }
@@ -603,9 +625,9 @@ slope_status slope_device_status(void* stream, int* site) {
 slope_status slope_debug_timeout_selftest(uint64_t limit_ns, void* stream) {
   if (limit_ns < 1000ull || limit_ns > 5000000000ull) return SLOPE_ERR_SHAPE;
   int* ptr = device_status_ptr();
-  if (ptr == nullptr) return SLOPE_ERR_CUDA;
-  return launch_timeout_selftest(limit_ns, ptr, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SLOPE_OK
-                                                                                                   : SLOPE_ERR_CUDA;
+  if (ptr == nullptr) return cuda_fail("device status word (cudaGetSymbolAddress)");
+  const cudaError_t e = launch_timeout_selftest(limit_ns, ptr, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SLOPE_OK : cuda_fail("self-test kernel launch", e);
 }
 
 const char* slope_status_string(slope_status s) {
@@ -625,5 +647,7 @@ const char* slope_status_string(slope_status s) {
 }
 
 const char* slope_version(void) { return "slope-gb300 0.1.0 (sm_103a)"; }
+
+const char* slope_last_error(void) { return g_last_error; }
 
 }  // extern "C"

@@ -9,19 +9,25 @@
 // by the log-sum-exp merge.
 //
 // Structure (one CTA = one item x 256 query rows x one query head):
-//   warp 0      TMA producer: Q tiles once, then K and V tiles through a ring
+//   warps 0-3   online softmax of Q tile 0 (one query row per thread = TMEM lane),
+//   warps 4-7   online softmax of Q tile 1; each also runs its tile's epilogue.
+//   warp 8      TMA producer: Q tiles once, then K and V tiles through a ring
 //               of shared-memory slots (128-byte swizzle, 64-column chunks).
-//   warp 1      MMA issuer: S_t = Q_t K^T (SS, K-major) into TMEM, then
-//               O_t += P_t V (P from TMEM, V MN-major) for the two Q tiles.
-//   warp 2      owns the 512-column TMEM allocation.
-//   warps 4-7   online softmax of Q tile 0 (one query row per thread = TMEM lane),
-//   warps 8-11  online softmax of Q tile 1; each also runs its tile's epilogue.
+//   warp 9      MMA issuer: S_t = Q_t K^T (SS, K-major) into TMEM, then
+//               O_t += P_t V (P from TMEM, V MN-major) for the two Q tiles;
+//               it also owns the 512-column TMEM allocation.
+//   warps 10-11 idle.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+dv), O_1 after it.
-// P_t (bf16 pairs) overwrites the first 64 columns of S_t after S_t is read.
+// With dv = 64 the last 128 columns hold P_0 and P_1 (bf16 pairs, 64 columns
+// each), so the MMA warp issues S(n+1) = Q K(n+1)^T before O += P(n) V(n) and
+// the softmax of step n+1 starts while PV(n) still runs.  With dv = 128 TMEM is
+// full: P_t overwrites the first 64 columns of S_t, and S(n+1) waits for PV(n).
 // Scores live in the log2 domain (scale * log2 e folded into one FMA); the
 // running max is only moved when it grows by more than 8 (factor 256), which
 // keeps every p <= 256 and makes most O rescales unnecessary; the final
 // normalisation uses the same max, so the result is exact either way.
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "sm103_ptx.cuh"
 #include "waits.cuh"
@@ -30,6 +36,10 @@ namespace slope {
 namespace {
 
 constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 64 bf16 (128 bytes)
+constexpr int kTmaWarp = 4 * kQTiles;        // warps 0..7 are the two softmax warpgroups
+constexpr int kMmaWarp = kTmaWarp + 1;
+// 12 warps put 3 warps on each SM sub-partition (16K registers each), which caps
+// a thread at 168 registers.
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 
@@ -43,12 +53,16 @@ struct K1Cfg {
   static constexpr int kVTileBytes = kVChunks * kChunkBytes;
   static constexpr int kSlotBytes = kKTileBytes > kVTileBytes ? kKTileBytes : kVTileBytes;
   static constexpr int kSlots = DQK == 64 ? 8 : (DQK == 128 ? 4 : 2);
-  static constexpr int kNumBars = 1 + 2 * kSlots + 3 * kQTiles + 1;
+  static constexpr int kNumBars = 1 + 2 * kSlots + 4 * kQTiles + 2;
   static constexpr int kBarOffset = kQTiles * kQTileBytes + kSlots * kSlotBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 8 * kNumBars + 16;
   static constexpr uint32_t kColO = 256;
+  static constexpr uint32_t kColP = kColO + kQTiles * DV;           // separate P columns, if they fit
+  static constexpr bool kSepP = kColP + kQTiles * (kBlockN / 2) <= 512;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kColO + kQTiles * DV <= 512, "TMEM budget");
+  // TMEM column of P_t
+  __device__ static constexpr uint32_t col_p(int t) { return kSepP ? kColP + t * (kBlockN / 2) : t * kBlockN; }
 };
 
 __device__ __forceinline__ int floor_div(int a, int b) {
@@ -109,6 +123,32 @@ __device__ __forceinline__ bool for_each_step(const WorkItem& it, const AttnPara
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
+// One unit of work: an item's 256-row block for one query head.
+struct Tile {
+  WorkItem itm;
+  int blk, h, g;
+  TileGeom geo;
+};
+
+// Work tile w -> (item, row block, head).  Consecutive w are the heads of one row
+// block (K/V shared in L2 by a KV group); items come heaviest first and an item's
+// later (heavier under the causal mask) row blocks before its earlier ones.
+__device__ __forceinline__ void decode_tile(const AttnParams& p, int w, Tile& T) {
+  int ii = 0;
+  while (ii < p.n_items - 1 && w >= (p.items[ii].cta_begin + p.items[ii].n_blocks) * p.Hq) ++ii;
+  T.itm = p.items[ii];
+  const int local = w - T.itm.cta_begin * p.Hq;
+  T.blk = T.itm.n_blocks - 1 - local / p.Hq;
+  T.h = local % p.Hq;
+  T.g = T.h / p.group;
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    T.geo.rows[t] = max(0, min(kBlockM, T.itm.q_len - T.blk * kRowsPerCta - t * kBlockM));
+    T.geo.qa[t] = p.q_pos_off + T.itm.q_row0 + T.blk * kRowsPerCta + t * kBlockM;
+    T.geo.qb[t] = T.geo.qa[t] + T.geo.rows[t] - 1;
+  }
+}
+
 template <int DQK, int DV>
 __global__ void __launch_bounds__(kK1Threads, 1)
     attn_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -125,39 +165,25 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   uint64_t* bar_s = bar_empty + C::kSlots;
   uint64_t* bar_p = bar_s + kQTiles;
   uint64_t* bar_o = bar_p + kQTiles;
-  uint64_t* bar_drain = bar_o + kQTiles;
+  uint64_t* bar_ofree = bar_o + kQTiles;
+  uint64_t* bar_qempty = bar_ofree + kQTiles;
+  uint64_t* bar_drain = bar_qempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + 1);
   volatile int* cta_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- which item / row block / head this CTA computes
-  const int bid = blockIdx.x;
-  int ii = 0;
-  while (ii < p.n_items - 1 && bid >= (p.items[ii].cta_begin + p.items[ii].n_blocks) * p.Hq) ++ii;
-  const WorkItem itm = p.items[ii];
-  const int local = bid - itm.cta_begin * p.Hq;
-  const int blk = itm.n_blocks - 1 - local / p.Hq;  // heavier (later) row blocks first
-  const int h = local % p.Hq;
-  const int g = h / p.group;
-  TileGeom geo;
-#pragma unroll
-  for (int t = 0; t < kQTiles; ++t) {
-    geo.rows[t] = max(0, min(kBlockM, itm.q_len - blk * kRowsPerCta - t * kBlockM));
-    geo.qa[t] = p.q_pos_off + itm.q_row0 + blk * kRowsPerCta + t * kBlockM;
-    geo.qb[t] = geo.qa[t] + geo.rows[t] - 1;
-  }
+  const int total = p.total_tiles;
 
   // ---- a CTA scheduled after a timeout elsewhere does nothing
   if (threadIdx.x == 0) *cta_abort = (*reinterpret_cast<volatile int*>(p.status) != 0) ? 1 : 0;
   __syncthreads();
   if (*cta_abort) return;
 
-  if (warp == 2) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  if (threadIdx.x == 32) {
+  if (threadIdx.x == kMmaWarp * 32) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(&bar_full[s], 1);
@@ -167,11 +193,13 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       mbar_init(&bar_s[t], 1);
       mbar_init(&bar_p[t], 4);
       mbar_init(&bar_o[t], 1);
+      mbar_init(&bar_ofree[t], 4);
     }
+    mbar_init(bar_qempty, 1);
     mbar_init(bar_drain, 1);
     fence_barrier_init();
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == kTmaWarp * 32) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
@@ -182,55 +210,133 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint64_t limit = p.wait_limit_ns;
 
-  if (warp == 0) {
+  if (warp == kTmaWarp) {
     // ================================================================ TMA producer
     if (lane == 0) {
-      const int nq = geo.rows[1] > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(bar_q, nq * C::kQTileBytes);
-      for (int t = 0; t < nq; ++t)
-        for (int c = 0; c < C::kQChunks; ++c)
-          tma_load_3d(sQ + t * C::kQTileBytes + c * kChunkBytes, &tm_q, bar_q, 64 * c, h,
-                      itm.q_row0 + blk * kRowsPerCta + t * kBlockM);
       uint32_t cnt = 0;
-      const bool ok = for_each_step(itm, p, geo, [&](const Step& s) -> bool {
-        {  // K tile
-          const uint32_t slot = cnt % C::kSlots, ph = (cnt / C::kSlots) & 1;
-          if (!wait_bounded(&bar_empty[slot], ph ^ 1, cta_abort, p.status, limit, 1)) return false;
-          mbar_arrive_expect_tx(&bar_full[slot], C::kKTileBytes);
+      int wt = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < total; w += gridDim.x) {
+        Tile T;
+        decode_tile(p, w, T);
+        // Q of the previous work tile is in use until its last S MMAs are done
+        if (wt > 0 && !wait_bounded(bar_qempty, (wt - 1) & 1, cta_abort, p.status, limit, 11)) {
+          ok = false;
+          break;
+        }
+        const int nq = T.geo.rows[1] > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(bar_q, nq * C::kQTileBytes);
+        for (int t = 0; t < nq; ++t)
           for (int c = 0; c < C::kQChunks; ++c)
-            tma_load_3d(sSlot + slot * C::kSlotBytes + c * kChunkBytes, &tm_k, &bar_full[slot], 64 * c, g, s.krow);
-          ++cnt;
-        }
-        {  // V tile
-          const uint32_t slot = cnt % C::kSlots, ph = (cnt / C::kSlots) & 1;
-          if (!wait_bounded(&bar_empty[slot], ph ^ 1, cta_abort, p.status, limit, 2)) return false;
-          mbar_arrive_expect_tx(&bar_full[slot], C::kVTileBytes);
-          for (int c = 0; c < C::kVChunks; ++c)
-            tma_load_3d(sSlot + slot * C::kSlotBytes + c * kChunkBytes, &tm_v, &bar_full[slot], 64 * c, g, s.krow);
-          ++cnt;
-        }
-        return true;
-      });
+            tma_load_3d(sQ + t * C::kQTileBytes + c * kChunkBytes, &tm_q, bar_q, 64 * c, T.h,
+                        T.itm.q_row0 + T.blk * kRowsPerCta + t * kBlockM);
+        ++wt;  // Q loads issued
+        ok = for_each_step(T.itm, p, T.geo, [&](const Step& s) -> bool {
+          {  // K tile
+            const uint32_t slot = cnt % C::kSlots, ph = (cnt / C::kSlots) & 1;
+            if (!wait_bounded(&bar_empty[slot], ph ^ 1, cta_abort, p.status, limit, 1)) return false;
+            mbar_arrive_expect_tx(&bar_full[slot], C::kKTileBytes);
+            for (int c = 0; c < C::kQChunks; ++c)
+              tma_load_3d(sSlot + slot * C::kSlotBytes + c * kChunkBytes, &tm_k, &bar_full[slot], 64 * c, T.g,
+                          s.krow);
+            ++cnt;
+          }
+          {  // V tile
+            const uint32_t slot = cnt % C::kSlots, ph = (cnt / C::kSlots) & 1;
+            if (!wait_bounded(&bar_empty[slot], ph ^ 1, cta_abort, p.status, limit, 2)) return false;
+            mbar_arrive_expect_tx(&bar_full[slot], C::kVTileBytes);
+            for (int c = 0; c < C::kVChunks; ++c)
+              tma_load_3d(sSlot + slot * C::kSlotBytes + c * kChunkBytes, &tm_v, &bar_full[slot], 64 * c, T.g,
+                          s.krow);
+            ++cnt;
+          }
+          return true;
+        });
+        if (!ok) break;
+      }
       if (!ok) {
         // let the loads already issued land before the CTA gives up its shared memory
-        wait_final(bar_q, 0, limit);
+        if (wt > 0) wait_final(bar_q, (wt - 1) & 1, limit);
         for (uint32_t s = 0; s < C::kSlots && s < cnt; ++s) {
           const uint32_t last = s + ((cnt - 1 - s) / C::kSlots) * C::kSlots;
           wait_final(&bar_full[s], (last / C::kSlots) & 1, limit);
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ================================================================ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, DV, 0, 1);
       uint32_t cnt = 0;
-      int n[kQTiles] = {0, 0};
-      if (wait_bounded(bar_q, 0, cta_abort, p.status, limit, 3)) {
+      int n[kQTiles] = {0, 0};    // S MMAs issued per Q tile, over all work tiles
+      int pvw[kQTiles] = {0, 0};  // work tiles whose first PV into O_t has been issued
+      // separate-P order: the PVs of the previous step, issued after this step's S MMAs
+      bool pend = false;
+      uint32_t pend_mask = 0, pend_first = 0, pend_vslot = 0, pend_vph = 0;
+      int pend_k[kQTiles] = {0, 0};
+
+      auto issue_qk = [&](int t, uint32_t kbase) {
+        const uint32_t qbase = smem_u32(sQ + t * C::kQTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem + t * kBlockN, smem_desc(qbase + off, 16, 1024, kSwizzle128B),
+                 smem_desc(kbase + off, 16, 1024, kSwizzle128B), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_s[t]);
+      };
+      // PV of tile t; the first PV of a work tile overwrites O_t, so it waits until the
+      // previous work tile's epilogue has read O_t
+      auto issue_pv = [&](int t, uint32_t vbase, bool first) -> bool {
+        if (first) {
+          if (pvw[t] > 0) {
+            if (!wait_bounded(&bar_ofree[t], (pvw[t] - 1) & 1, cta_abort, p.status, limit, 12)) return false;
+            tc_fence_after_sync();
+          }
+          ++pvw[t];
+        }
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          mma_ts(tmem + C::kColO + t * DV, tmem + C::col_p(t) + kk * 8,
+                 smem_desc(vbase + kk * 2048, kChunkBytes, 1024, kSwizzle128B), idesc_pv,
+                 (!first || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bar_o[t]);
+        return true;
+      };
+      auto flush = [&]() -> bool {
+        if (!pend) return true;
+        if (!wait_bounded(&bar_full[pend_vslot], pend_vph, cta_abort, p.status, limit, 6)) return false;
         tc_fence_after_sync();
-        for_each_step(itm, p, geo, [&](const Step& s) -> bool {
+        const uint32_t vbase = smem_u32(sSlot + pend_vslot * C::kSlotBytes);
+#pragma unroll
+        for (int t = 0; t < kQTiles; ++t) {
+          if (!((pend_mask >> t) & 1)) continue;
+          if (!wait_bounded(&bar_p[t], pend_k[t] & 1, cta_abort, p.status, limit, 7)) return false;
+          tc_fence_after_sync();
+          if (!issue_pv(t, vbase, (pend_first >> t) & 1)) return false;
+        }
+        mma_commit(&bar_empty[pend_vslot]);
+        pend = false;
+        return true;
+      };
+
+      bool ok = true;
+      int wt = 0;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++wt) {
+        Tile T;
+        decode_tile(p, w, T);
+        if (!wait_bounded(bar_q, wt & 1, cta_abort, p.status, limit, 3)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint32_t first_mask = (1u << kQTiles) - 1;  // Q tiles whose first PV of this work tile is still due
+        ok = for_each_step(T.itm, p, T.geo, [&](const Step& s) -> bool {
           const uint32_t kslot = cnt % C::kSlots, kph = (cnt / C::kSlots) & 1;
+          ++cnt;
+          const uint32_t vslot = cnt % C::kSlots, vph = (cnt / C::kSlots) & 1;
           ++cnt;
           if (!wait_bounded(&bar_full[kslot], kph, cta_abort, p.status, limit, 4)) return false;
           tc_fence_after_sync();
@@ -238,64 +344,73 @@ __global__ void __launch_bounds__(kK1Threads, 1)
 #pragma unroll
           for (int t = 0; t < kQTiles; ++t) {
             if (!((s.part >> t) & 1)) continue;
-            if (n[t] > 0) {  // S_t/P_t are free once the previous PV of tile t is done
-              if (!wait_bounded(&bar_o[t], (n[t] - 1) & 1, cta_abort, p.status, limit, 5)) return false;
+            if (n[t] > 0) {
+              // separate P: S_t is free once softmax t has read it (it then arrived on bar_p);
+              // P inside S_t: also wait until the previous PV has consumed P_t
+              uint64_t* b = C::kSepP ? &bar_p[t] : &bar_o[t];
+              if (!wait_bounded(b, (n[t] - 1) & 1, cta_abort, p.status, limit, 5)) return false;
               tc_fence_after_sync();
             }
-            const uint32_t qbase = smem_u32(sQ + t * C::kQTileBytes);
-#pragma unroll
-            for (int kk = 0; kk < DQK / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-              mma_ss(tmem + t * kBlockN, smem_desc(qbase + off, 16, 1024, kSwizzle128B),
-                     smem_desc(kbase + off, 16, 1024, kSwizzle128B), idesc_qk, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&bar_s[t]);
+            issue_qk(t, kbase);
           }
           mma_commit(&bar_empty[kslot]);
-
-          const uint32_t vslot = cnt % C::kSlots, vph = (cnt / C::kSlots) & 1;
-          ++cnt;
-          if (!wait_bounded(&bar_full[vslot], vph, cta_abort, p.status, limit, 6)) return false;
-          tc_fence_after_sync();
-          const uint32_t vbase = smem_u32(sSlot + vslot * C::kSlotBytes);
+          if (C::kSepP) {
+            if (!flush()) return false;
+            pend = true;
+            pend_mask = s.part;
+            pend_first = s.part & first_mask;
+            first_mask &= ~s.part;
+            pend_vslot = vslot;
+            pend_vph = vph;
 #pragma unroll
-          for (int t = 0; t < kQTiles; ++t) {
-            if (!((s.part >> t) & 1)) continue;
-            if (!wait_bounded(&bar_p[t], n[t] & 1, cta_abort, p.status, limit, 7)) return false;
+            for (int t = 0; t < kQTiles; ++t)
+              if ((s.part >> t) & 1) pend_k[t] = n[t]++;
+          } else {
+            if (!wait_bounded(&bar_full[vslot], vph, cta_abort, p.status, limit, 6)) return false;
             tc_fence_after_sync();
+            const uint32_t vbase = smem_u32(sSlot + vslot * C::kSlotBytes);
 #pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk) {
-              mma_ts(tmem + C::kColO + t * DV, tmem + t * kBlockN + kk * 8,
-                     smem_desc(vbase + kk * 2048, kChunkBytes, 1024, kSwizzle128B), idesc_pv,
-                     (n[t] > 0 || kk > 0) ? 1u : 0u);
+            for (int t = 0; t < kQTiles; ++t) {
+              if (!((s.part >> t) & 1)) continue;
+              if (!wait_bounded(&bar_p[t], n[t] & 1, cta_abort, p.status, limit, 7)) return false;
+              tc_fence_after_sync();
+              if (!issue_pv(t, vbase, (first_mask >> t) & 1)) return false;
+              first_mask &= ~(1u << t);
+              ++n[t];
             }
-            mma_commit(&bar_o[t]);
-            ++n[t];
+            mma_commit(&bar_empty[vslot]);
           }
-          mma_commit(&bar_empty[vslot]);
           return true;
         });
+        // every S MMA of this work tile is issued: Q may be reloaded once they are done
+        mma_commit(bar_qempty);
       }
+      if (ok) flush();
       // every MMA (and the arrivals its commits make) completes before teardown
       mma_commit(bar_drain);
       wait_final(bar_drain, 0, limit);
     }
-  } else if (warp >= 4) {
+  } else if (warp < kTmaWarp) {
     // ================================================================ softmax + epilogue
-    const int t = (warp - 4) >> 2;
+    const int t = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * kBlockN;
+    const uint32_t tP = tmem + lane_base + C::col_p(t);
     const uint32_t tO = tmem + lane_base + C::kColO + t * DV;
-    const int q_pos = geo.qa[t] + row;
     const float sl2 = p.scale_log2;
-    float m_used = -INFINITY;  // running max in log2-scaled units
-    float l = 0.f;             // running sum of exp2(s*sl2 - m_used)
-    int n = 0;
+    int n = 0;  // steps (= PVs) of this Q tile over all work tiles
     bool ok = true;
-    if (geo.rows[t] > 0) {
-      ok = for_each_step(itm, p, geo, [&](const Step& s) -> bool {
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      Tile T;
+      decode_tile(p, w, T);
+      if (T.geo.rows[t] <= 0) continue;
+      const int q_pos = T.geo.qa[t] + row;
+      float m_used = -INFINITY;  // running max in log2-scaled units
+      float l = 0.f;             // running sum of exp2(s*sl2 - m_used)
+      int nl = 0;                // steps of this work tile
+      ok = for_each_step(T.itm, p, T.geo, [&](const Step& s) -> bool {
         if (!((s.part >> t) & 1)) return true;
         if (!warp_all(wait_bounded(&bar_s[t], n & 1, cta_abort, p.status, limit, 8))) return false;
         tc_fence_after_sync();
@@ -325,9 +440,18 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             if (!vis) sv[c] = -INFINITY;
           }
         }
-        float mx = sv[0];
+        // row max: four independent chains of 3-input max
+        float a0 = sv[0], a1 = sv[1], a2 = sv[2], a3 = sv[3];
 #pragma unroll
-        for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, sv[c]);
+        for (int i = 4; i < 124; i += 8) {
+          a0 = fmax3(a0, sv[i], sv[i + 1]);
+          a1 = fmax3(a1, sv[i + 2], sv[i + 3]);
+          a2 = fmax3(a2, sv[i + 4], sv[i + 5]);
+          a3 = fmax3(a3, sv[i + 6], sv[i + 7]);
+        }
+        a0 = fmax3(a0, sv[124], sv[125]);
+        a1 = fmax3(a1, sv[126], sv[127]);
+        const float mx = fmax3(a0, a1, fmaxf(a2, a3));
         const float m_new = mx * sl2;
         const bool need = m_new > m_used + kRescaleThreshold;
         const bool any_need = __any_sync(0xffffffffu, need);
@@ -338,74 +462,93 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           l *= alpha;
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+        // p = exp2(s * sl2 - m), packed to bf16 pairs; row sum in fp32 (four packed chains)
+        const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-msub, -msub);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+        uint32_t pk[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2_approx(fmaf(sv[32 * c + 2 * i], sl2, -msub));
-            const float p1 = ex2_approx(fmaf(sv[32 * c + 2 * i + 1], sl2, -msub));
-            l += p0 + p1;
-            pk[i] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(tS + c * 16, pk);
+        for (int i = 0; i < 64; ++i) {
+          const float2 x = ffma2(make_float2(sv[2 * i], sv[2 * i + 1]), sl2v, negm);
+          const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+          acc[i & 3] = fadd2(acc[i & 3], make_float2(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st_wait();
-        if (any_need && n > 0) {  // rescale O_t once the previous PV into it has finished
+        const float2 acc01 = fadd2(acc[0], acc[1]), acc23 = fadd2(acc[2], acc[3]);
+        const float2 accs = fadd2(acc01, acc23);
+        l += accs.x + accs.y;
+        if (!C::kSepP) {  // P over S_t: every S value is already in registers
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * c]));
+        }
+        if ((C::kSepP && n > 0) || (any_need && nl > 0)) {
+          // the previous PV of this tile must be done before P_t is overwritten / O_t is rescaled
           if (!warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 9))) return false;
           tc_fence_after_sync();
+        }
+        if (C::kSepP) {
 #pragma unroll
-          for (int c = 0; c < DV / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
+          for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * c]));
+        }
+        if (any_need && nl > 0) {
+#pragma unroll 1
+          for (int c = 0; c < DV / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld16(tO + c * 16, o);
             tmem_ld_wait();
             reg_fence(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + c * 32, o);
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st16(tO + c * 16, o);
           }
-          tmem_st_wait();
         }
+        tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p[t]);
         ++n;
+        ++nl;
         return true;
       });
+      if (!ok) break;
 
       // ---- epilogue: out = O / l, lse = ln(sum exp(scaled scores))
-      if (ok && n > 0) ok = warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 10));
-      if (ok) {
-        const bool valid_row = row < geo.rows[t];
-        const int64_t orow = static_cast<int64_t>(itm.out_row0) + blk * kRowsPerCta + t * kBlockM + row;
-        float* op = p.out + static_cast<int64_t>(itm.plane) * p.out_splane + orow * p.out_srow +
-                    static_cast<int64_t>(h) * p.out_shead;
-        if (n > 0) {
-          tc_fence_after_sync();
-          const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (nl > 0) ok = warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 10));
+      if (!ok) break;
+      const bool valid_row = row < T.geo.rows[t];
+      const int64_t orow = static_cast<int64_t>(T.itm.out_row0) + T.blk * kRowsPerCta + t * kBlockM + row;
+      float* op = p.out + static_cast<int64_t>(T.itm.plane) * p.out_splane + orow * p.out_srow +
+                  static_cast<int64_t>(T.h) * p.out_shead;
+      if (nl > 0) {
+        tc_fence_after_sync();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-          for (int c = 0; c < DV / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait();
-            reg_fence(o);
-            if (valid_row) {
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait();
+          reg_fence(o);
+          if (c == DV / 32 - 1) {  // O_t is read: the next work tile's first PV may overwrite it
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_ofree[t]);
+          }
+          if (valid_row) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                       __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-                *reinterpret_cast<float4*>(op + c * 32 + 4 * i) = v;
-              }
+            for (int i = 0; i < 8; ++i) {
+              float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                     __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+              *reinterpret_cast<float4*>(op + c * 32 + 4 * i) = v;
             }
           }
-        } else if (p.write_empty_out && valid_row) {
+        }
+      } else if (p.write_empty_out && valid_row) {
 #pragma unroll
-          for (int i = 0; i < DV / 4; ++i) *reinterpret_cast<float4*>(op + 4 * i) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        if (valid_row) {
-          p.lse[static_cast<int64_t>(itm.plane) * p.lse_splane + orow * p.lse_srow +
-                static_cast<int64_t>(h) * p.lse_shead] = l > 0.f ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
-        }
+        for (int i = 0; i < DV / 4; ++i) *reinterpret_cast<float4*>(op + 4 * i) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (valid_row) {
+        p.lse[static_cast<int64_t>(T.itm.plane) * p.lse_splane + orow * p.lse_srow +
+              static_cast<int64_t>(T.h) * p.lse_shead] = l > 0.f ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
       }
     }
   }
@@ -413,25 +556,37 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   __syncwarp();
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
 }
 
+// CTAs per launch: one persistent CTA per SM (each holds the SM's whole TMEM),
+// or fewer when there are fewer work tiles.
+int resident_ctas() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return 1;
+  return sms;
+}
+
 template <int DQK, int DV>
-cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, AttnParams p,
                         cudaStream_t stream) {
   using C = K1Cfg<DQK, DV>;
   if (p.n_items <= 0) return cudaSuccess;
   const WorkItem& last = p.items[p.n_items - 1];
-  const long long ctas = static_cast<long long>(last.cta_begin + last.n_blocks) * p.Hq;
-  if (ctas <= 0) return cudaSuccess;
-  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const long long tiles = static_cast<long long>(last.cta_begin + last.n_blocks) * p.Hq;
+  if (tiles <= 0) return cudaSuccess;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  p.total_tiles = static_cast<int32_t>(tiles);
+  const long long grid = std::min<long long>(tiles, resident_ctas());
   cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_partial_kernel<DQK, DV><<<static_cast<unsigned>(ctas), kK1Threads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  attn_partial_kernel<DQK, DV><<<static_cast<unsigned>(grid), kK1Threads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -13,7 +13,7 @@ constexpr int kBlockM = 128;      // query rows per Q tile (= TMEM lanes)
 constexpr int kBlockN = 128;      // keys per K/V tile
 constexpr int kQTiles = 2;        // Q tiles per CTA; they share every K/V tile
 constexpr int kRowsPerCta = kBlockM * kQTiles;
-constexpr int kK1Threads = 384;   // warp 0 TMA, warp 1 MMA, warp 2 TMEM owner, 4..11 softmax
+constexpr int kK1Threads = 384;   // warps 0..7 softmax (two warpgroups), 8 TMA, 9 MMA + TMEM owner, 10-11 idle
 constexpr int kMaxItems = 32;     // work items per launch
 constexpr int kMaxKvRanges = 2;   // key/value ranges per item
 
@@ -36,6 +36,7 @@ struct WorkItem {
 
 struct AttnParams {
   int32_t n_items;
+  int32_t total_tiles;      // work tiles (item row blocks x query heads); set by the launcher
   int32_t Hq;
   int32_t group;            // Hq / Hkv
   int32_t causal;

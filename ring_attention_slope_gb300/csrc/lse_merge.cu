@@ -7,10 +7,10 @@
 //   L   = m + log sum_k exp(lse_k - m),  m = max_k lse_k   (all -inf -> -inf)
 //   out = sum_k exp(lse_k - L) * out_k   (partials with lse_k = -inf are not read)
 //
-// Bandwidth-bound: each thread owns 4 consecutive output elements of one
-// (row, head); it reads the n log-sum-exp values of its row first, then issues
-// the (predicated) 16-byte streaming loads of all live partials in batches of
-// 8 so that many loads are in flight, and writes bf16 or fp32.
+// Bandwidth-bound: four threads share one (row, head); each reads the n
+// log-sum-exp values of the row, then issues predicated 16-byte streaming
+// loads of its quarter of every live partial in batches of four partials, so
+// many loads are in flight per thread, and writes bf16 or fp32.
 #include <cuda_bf16.h>
 
 #include "kernels.cuh"
@@ -24,13 +24,16 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int DV, bool OUT_BF16>
 __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const __grid_constant__ MergeParams p) {
-  constexpr int kTpr = DV / 4;  // threads per (row, head)
+  // 4 threads per (row, head); thread q owns float4 columns q, q+4, q+8, ... so that each
+  // load instruction of a warp reads 8 contiguous 64-byte runs.
+  constexpr int kTpp = 4;
+  constexpr int kVec = DV / 4 / kTpp;  // float4s per thread per partial
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kMergeThreads + threadIdx.x;
-  const int64_t pair = gtid / kTpr;
-  const int c4 = static_cast<int>(gtid % kTpr);
+  const int64_t pair = gtid >> 2;
+  const int q = static_cast<int>(gtid & 3);
   if (pair >= p.S * p.H) return;
   const int64_t row = pair / p.H;
-  const int h = static_cast<int>(pair % p.H);
+  const int h = static_cast<int>(pair - row * p.H);
 
   float lk[kMaxMerge];
   float mx = -INFINITY;
@@ -43,7 +46,9 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const __grid_c
     }
   }
 
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc[kVec];
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = -INFINITY;
   if (mx != -INFINITY) {
     float sum = 0.f;
@@ -52,42 +57,51 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const __grid_c
       if (k < p.n) sum += ex2_approx((lk[k] - mx) * kLog2e);
     L = mx + lg2_approx(sum) * kLn2;
 #pragma unroll
-    for (int b = 0; b < kMaxMerge; b += 8) {
+    for (int b = 0; b < kMaxMerge; b += 4) {
       if (b >= p.n) break;
-      float4 v[8];
-      float w[8];
+      float4 v[4][kVec];
+      float w[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int k = b + i;
         const bool live = k < p.n && lk[k] != -INFINITY;
         w[i] = live ? ex2_approx((lk[k] - L) * kLog2e) : 0.f;
-        v[i] = live ? __ldcs(reinterpret_cast<const float4*>(p.outs[k] + row * p.o_srow[k] + h * p.o_shead[k]) + c4)
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4* src = live ? reinterpret_cast<const float4*>(p.outs[k] + row * p.o_srow[k] + h * p.o_shead[k])
+                                 : nullptr;
+#pragma unroll
+        for (int j = 0; j < kVec; ++j)
+          v[i][j] = live ? __ldcs(src + q + kTpp * j) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        acc.x = fmaf(w[i], v[i].x, acc.x);
-        acc.y = fmaf(w[i], v[i].y, acc.y);
-        acc.z = fmaf(w[i], v[i].z, acc.z);
-        acc.w = fmaf(w[i], v[i].w, acc.w);
-      }
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+          acc[j].x = fmaf(w[i], v[i][j].x, acc[j].x);
+          acc[j].y = fmaf(w[i], v[i][j].y, acc[j].y);
+          acc[j].z = fmaf(w[i], v[i][j].z, acc[j].z);
+          acc[j].w = fmaf(w[i], v[i][j].w, acc[j].w);
+        }
     }
   }
 
-  if (OUT_BF16) {
-    __nv_bfloat16* base = static_cast<__nv_bfloat16*>(p.out);
-    uint2 packed = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-    *reinterpret_cast<uint2*>(base + row * p.out_srow + h * p.out_shead + 4 * c4) = packed;
-  } else {
-    float* base = static_cast<float*>(p.out);
-    *reinterpret_cast<float4*>(base + row * p.out_srow + h * p.out_shead + 4 * c4) = acc;
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    const int64_t col = 4 * (q + kTpp * j);
+    if (OUT_BF16) {
+      __nv_bfloat16* base = static_cast<__nv_bfloat16*>(p.out);
+      const uint2 packed = make_uint2(pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j].z, acc[j].w));
+      *reinterpret_cast<uint2*>(base + row * p.out_srow + h * p.out_shead + col) = packed;
+    } else {
+      float* base = static_cast<float*>(p.out);
+      *reinterpret_cast<float4*>(base + row * p.out_srow + h * p.out_shead + col) = acc[j];
+    }
   }
-  if (c4 == 0 && p.lse != nullptr) p.lse[row * p.lse_srow + h * p.lse_shead] = L;
+  if (q == 0 && p.lse != nullptr) p.lse[row * p.lse_srow + h * p.lse_shead] = L;
 }
 
 template <int DV, bool BF16>
 cudaError_t launch_impl(const MergeParams& p, cudaStream_t stream) {
-  const int64_t threads = p.S * p.H * (DV / 4);
+  const int64_t threads = p.S * p.H * 4;
   if (threads == 0) return cudaSuccess;
   const int64_t blocks = (threads + kMergeThreads - 1) / kMergeThreads;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
