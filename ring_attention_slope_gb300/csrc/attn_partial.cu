@@ -92,7 +92,9 @@ __device__ __forceinline__ bool for_each_step(const WorkItem& it, const AttnPara
   const int qa_min = g.qa[0];
   const int qb_max = g.rows[1] > 0 ? g.qb[1] : g.qb[0];
   for (int r = 0; r < it.n_kv; ++r) {
-    const int row0 = it.kv[r].row0, len = it.kv[r].len;
+    // select instead of a dynamic index: keeps the ranges in registers
+    const int row0 = r == 0 ? it.kv[0].row0 : it.kv[1].row0;
+    const int len = r == 0 ? it.kv[0].len : it.kv[1].len;
     const int kpos0 = p.kv_pos_off + row0;
     int lo = 0, hi = (len + kBlockN - 1) / kBlockN - 1;
     if (p.causal) hi = min(hi, floor_div(qb_max - kpos0, kBlockN));
@@ -265,30 +267,35 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issuer
+    // Per step j, for each Q tile t in turn: S_t(j) = Q_t K(j)^T, then (separate-P
+    // layout) O_t += P_t(j-1) V(j-1), so each tile's PV follows its own S MMA and
+    // the other tile's softmax overlaps both.  With P inside S_t (dv = 128) the PV
+    // of step j follows S_t(j) directly once softmax t has written P_t(j).
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, DV, 0, 1);
+      constexpr uint32_t kDescHi = smem_desc_hi(1024, kSwizzle128B);
       uint32_t cnt = 0;
       int n[kQTiles] = {0, 0};    // S MMAs issued per Q tile, over all work tiles
       int pvw[kQTiles] = {0, 0};  // work tiles whose first PV into O_t has been issued
-      // separate-P order: the PVs of the previous step, issued after this step's S MMAs
+      // separate-P order: the PVs of the previous step
       bool pend = false;
       uint32_t pend_mask = 0, pend_first = 0, pend_vslot = 0, pend_vph = 0;
       int pend_k[kQTiles] = {0, 0};
 
-      auto issue_qk = [&](int t, uint32_t kbase) {
-        const uint32_t qbase = smem_u32(sQ + t * C::kQTileBytes);
+      auto issue_qk = [&](int t, uint32_t kslot) {
+        const uint32_t qlo = smem_desc_lo(smem_u32(sQ + t * C::kQTileBytes), 16);
+        const uint32_t klo = smem_desc_lo(smem_u32(sSlot + kslot * C::kSlotBytes), 16);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + t * kBlockN, smem_desc(qbase + off, 16, 1024, kSwizzle128B),
-                 smem_desc(kbase + off, 16, 1024, kSwizzle128B), idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss_lh(tmem + t * kBlockN, qlo + off, kDescHi, klo + off, kDescHi, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar_s[t]);
       };
       // PV of tile t; the first PV of a work tile overwrites O_t, so it waits until the
       // previous work tile's epilogue has read O_t
-      auto issue_pv = [&](int t, uint32_t vbase, bool first) -> bool {
+      auto issue_pv = [&](int t, uint32_t vslot, bool first) -> bool {
         if (first) {
           if (pvw[t] > 0) {
             if (!wait_bounded(&bar_ofree[t], (pvw[t] - 1) & 1, cta_abort, p.status, limit, 12)) return false;
@@ -296,29 +303,13 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           }
           ++pvw[t];
         }
+        const uint32_t vlo = smem_desc_lo(smem_u32(sSlot + vslot * C::kSlotBytes), kChunkBytes);
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          mma_ts(tmem + C::kColO + t * DV, tmem + C::col_p(t) + kk * 8,
-                 smem_desc(vbase + kk * 2048, kChunkBytes, 1024, kSwizzle128B), idesc_pv,
-                 (!first || kk > 0) ? 1u : 0u);
+          mma_ts_lh(tmem + C::kColO + t * DV, tmem + C::col_p(t) + kk * 8, vlo + ((kk * 2048) >> 4), kDescHi,
+                    idesc_pv, (!first || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bar_o[t]);
-        return true;
-      };
-      auto flush = [&]() -> bool {
-        if (!pend) return true;
-        if (!wait_bounded(&bar_full[pend_vslot], pend_vph, cta_abort, p.status, limit, 6)) return false;
-        tc_fence_after_sync();
-        const uint32_t vbase = smem_u32(sSlot + pend_vslot * C::kSlotBytes);
-#pragma unroll
-        for (int t = 0; t < kQTiles; ++t) {
-          if (!((pend_mask >> t) & 1)) continue;
-          if (!wait_bounded(&bar_p[t], pend_k[t] & 1, cta_abort, p.status, limit, 7)) return false;
-          tc_fence_after_sync();
-          if (!issue_pv(t, vbase, (pend_first >> t) & 1)) return false;
-        }
-        mma_commit(&bar_empty[pend_vslot]);
-        pend = false;
         return true;
       };
 
@@ -339,23 +330,30 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           const uint32_t vslot = cnt % C::kSlots, vph = (cnt / C::kSlots) & 1;
           ++cnt;
           if (!wait_bounded(&bar_full[kslot], kph, cta_abort, p.status, limit, 4)) return false;
+          if (C::kSepP && pend && !wait_bounded(&bar_full[pend_vslot], pend_vph, cta_abort, p.status, limit, 6))
+            return false;
           tc_fence_after_sync();
-          const uint32_t kbase = smem_u32(sSlot + kslot * C::kSlotBytes);
 #pragma unroll
           for (int t = 0; t < kQTiles; ++t) {
-            if (!((s.part >> t) & 1)) continue;
-            if (n[t] > 0) {
-              // separate P: S_t is free once softmax t has read it (it then arrived on bar_p);
-              // P inside S_t: also wait until the previous PV has consumed P_t
+            const bool part = (s.part >> t) & 1;
+            const bool pv_due = C::kSepP && pend && ((pend_mask >> t) & 1);
+            if (part && n[t] > 0) {
+              // separate P: S_t is free once softmax t has read it (it then arrived on bar_p,
+              // which also releases P_t(j-1) for its PV); P inside S_t: wait until the
+              // previous PV has consumed P_t
               uint64_t* b = C::kSepP ? &bar_p[t] : &bar_o[t];
               if (!wait_bounded(b, (n[t] - 1) & 1, cta_abort, p.status, limit, 5)) return false;
               tc_fence_after_sync();
+            } else if (pv_due) {
+              if (!wait_bounded(&bar_p[t], pend_k[t] & 1, cta_abort, p.status, limit, 7)) return false;
+              tc_fence_after_sync();
             }
-            issue_qk(t, kbase);
+            if (part) issue_qk(t, kslot);
+            if (pv_due && !issue_pv(t, pend_vslot, (pend_first >> t) & 1)) return false;
           }
           mma_commit(&bar_empty[kslot]);
           if (C::kSepP) {
-            if (!flush()) return false;
+            if (pend) mma_commit(&bar_empty[pend_vslot]);
             pend = true;
             pend_mask = s.part;
             pend_first = s.part & first_mask;
@@ -368,13 +366,12 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           } else {
             if (!wait_bounded(&bar_full[vslot], vph, cta_abort, p.status, limit, 6)) return false;
             tc_fence_after_sync();
-            const uint32_t vbase = smem_u32(sSlot + vslot * C::kSlotBytes);
 #pragma unroll
             for (int t = 0; t < kQTiles; ++t) {
               if (!((s.part >> t) & 1)) continue;
               if (!wait_bounded(&bar_p[t], n[t] & 1, cta_abort, p.status, limit, 7)) return false;
               tc_fence_after_sync();
-              if (!issue_pv(t, vbase, (first_mask >> t) & 1)) return false;
+              if (!issue_pv(t, vslot, (first_mask >> t) & 1)) return false;
               first_mask &= ~(1u << t);
               ++n[t];
             }
@@ -385,7 +382,19 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         // every S MMA of this work tile is issued: Q may be reloaded once they are done
         mma_commit(bar_qempty);
       }
-      if (ok) flush();
+      if (ok && pend) {  // PVs of the last step
+        if (wait_bounded(&bar_full[pend_vslot], pend_vph, cta_abort, p.status, limit, 6)) {
+          tc_fence_after_sync();
+#pragma unroll
+          for (int t = 0; t < kQTiles; ++t) {
+            if (!((pend_mask >> t) & 1)) continue;
+            if (!wait_bounded(&bar_p[t], pend_k[t] & 1, cta_abort, p.status, limit, 7)) break;
+            tc_fence_after_sync();
+            if (!issue_pv(t, pend_vslot, (pend_first >> t) & 1)) break;
+          }
+          mma_commit(&bar_empty[pend_vslot]);
+        }
+      }
       // every MMA (and the arrivals its commits make) completes before teardown
       mma_commit(bar_drain);
       wait_final(bar_drain, 0, limit);
@@ -405,8 +414,9 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       Tile T;
       decode_tile(p, w, T);
-      if (T.geo.rows[t] <= 0) continue;
-      const int q_pos = T.geo.qa[t] + row;
+      const int rows_t = t == 0 ? T.geo.rows[0] : T.geo.rows[1];
+      if (rows_t <= 0) continue;
+      const int q_pos = (t == 0 ? T.geo.qa[0] : T.geo.qa[1]) + row;
       float m_used = -INFINITY;  // running max in log2-scaled units
       float l = 0.f;             // running sum of exp2(s*sl2 - m_used)
       int nl = 0;                // steps of this work tile
@@ -515,7 +525,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       // ---- epilogue: out = O / l, lse = ln(sum exp(scaled scores))
       if (nl > 0) ok = warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 10));
       if (!ok) break;
-      const bool valid_row = row < T.geo.rows[t];
+      const bool valid_row = row < rows_t;
       const int64_t orow = static_cast<int64_t>(T.itm.out_row0) + T.blk * kRowsPerCta + t * kBlockM + row;
       float* op = p.out + static_cast<int64_t>(T.itm.plane) * p.out_splane + orow * p.out_srow +
                   static_cast<int64_t>(T.h) * p.out_shead;

@@ -9,6 +9,9 @@
 
 namespace slope {
 
+// Longest hardware sleep per try_wait (the thread wakes as soon as the phase completes).
+constexpr uint32_t kWaitSleepNs = 100000;
+
 __device__ __forceinline__ void record_timeout(int* status, int site) {
   if (atomicCAS(status, 0, kStatusTimeout) == 0) atomicExch(status + 1, site);
 }
@@ -21,7 +24,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*cta_abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       *cta_abort = 1;
@@ -35,7 +38,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
 // already in flight land before the CTA releases its resources.
 __device__ __forceinline__ bool wait_final(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) {
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
