@@ -13,10 +13,10 @@
 //   warps 4-7   online softmax of Q tile 1; each also runs its tile's epilogue.
 //   warp 8      TMA producer: Q tiles once, then K and V tiles through a ring
 //               of shared-memory slots (128-byte swizzle, 64-column chunks).
-//   warp 9      MMA issuer: S_t = Q_t K^T (SS, K-major) into TMEM, then
-//               O_t += P_t V (P from TMEM, V MN-major) for the two Q tiles;
-//               it also owns the 512-column TMEM allocation.
-//   warps 10-11 idle.
+//   warps 9-10  MMA issuers, one per Q tile: S_t = Q_t K^T (SS, K-major) into
+//               TMEM, then O_t += P_t V (P from TMEM, V MN-major); warp 9 also
+//               owns the 512-column TMEM allocation.
+//   warp 11     idle.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+dv), O_1 after it.
 // With dv = 64 the last 128 columns hold P_0 and P_1 (bf16 pairs, 64 columns
 // each), so the MMA warp issues S(n+1) = Q K(n+1)^T before O += P(n) V(n) and
@@ -53,7 +53,7 @@ struct K1Cfg {
   static constexpr int kVTileBytes = kVChunks * kChunkBytes;
   static constexpr int kSlotBytes = kKTileBytes > kVTileBytes ? kKTileBytes : kVTileBytes;
   static constexpr int kSlots = DQK == 64 ? 8 : (DQK == 128 ? 4 : 2);
-  static constexpr int kNumBars = 1 + 2 * kSlots + 4 * kQTiles + 2;
+  static constexpr int kNumBars = 1 + 2 * kSlots + 5 * kQTiles + 1;
   static constexpr int kBarOffset = kQTiles * kQTileBytes + kSlots * kSlotBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 8 * kNumBars + 16;
   static constexpr uint32_t kColO = 256;
@@ -169,8 +169,8 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   uint64_t* bar_o = bar_p + kQTiles;
   uint64_t* bar_ofree = bar_o + kQTiles;
   uint64_t* bar_qempty = bar_ofree + kQTiles;
-  uint64_t* bar_drain = bar_qempty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + 1);
+  uint64_t* bar_drain = bar_qempty + 1;  // one per MMA issuer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + kQTiles);
   volatile int* cta_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     mbar_init(bar_q, 1);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_empty[s], kQTiles);  // one commit per MMA issuer
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(&bar_s[t], 1);
@@ -197,8 +197,8 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       mbar_init(&bar_o[t], 1);
       mbar_init(&bar_ofree[t], 4);
     }
-    mbar_init(bar_qempty, 1);
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_qempty, kQTiles);
+    for (int t = 0; t < kQTiles; ++t) mbar_init(&bar_drain[t], 1);
     fence_barrier_init();
   }
   if (threadIdx.x == kTmaWarp * 32) {
@@ -265,51 +265,68 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ================================================================ MMA issuer
-    // Per step j, for each Q tile t in turn: S_t(j) = Q_t K(j)^T, then (separate-P
-    // layout) O_t += P_t(j-1) V(j-1), so each tile's PV follows its own S MMA and
-    // the other tile's softmax overlaps both.  With P inside S_t (dv = 128) the PV
-    // of step j follows S_t(j) directly once softmax t has written P_t(j).
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ================================================================ MMA issuers
+    // One issuing thread per Q tile (warps on different SM sub-partitions), so each
+    // tile's MMAs wait only on that tile's softmax.  Per step j issuer t issues
+    // S_t(j) = Q_t K(j)^T and then (separate-P layout) O_t += P_t(j-1) V(j-1); with
+    // P inside S_t (dv = 128) O_t += P_t(j) V(j) once softmax t has written P_t(j).
+    // Every issuer commits once per K/V fill and per work tile (those barriers
+    // count one arrival per issuer), whether or not its tile used the step.
     if (lane == 0) {
+      const int t = warp - kMmaWarp;
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, DV, 0, 1);
       constexpr uint32_t kDescHi = smem_desc_hi(1024, kSwizzle128B);
+      const uint32_t qlo = smem_desc_lo(smem_u32(sQ + t * C::kQTileBytes), 16);
+      const uint32_t d_s = tmem + t * kBlockN, d_o = tmem + C::kColO + t * DV, a_p = tmem + C::col_p(t);
       uint32_t cnt = 0;
-      int n[kQTiles] = {0, 0};    // S MMAs issued per Q tile, over all work tiles
-      int pvw[kQTiles] = {0, 0};  // work tiles whose first PV into O_t has been issued
-      // separate-P order: the PVs of the previous step
-      bool pend = false;
-      uint32_t pend_mask = 0, pend_first = 0, pend_vslot = 0, pend_vph = 0;
-      int pend_k[kQTiles] = {0, 0};
+      int n = 0;    // S MMAs issued for this tile, over all work tiles
+      int pvw = 0;  // work tiles whose first PV into O_t has been issued
+      // separate-P order: the previous step's V slot and whether this tile used it
+      bool pend = false, pend_part = false, pend_first = false;
+      uint32_t pend_vslot = 0, pend_vph = 0;
+      int pend_k = 0;
 
-      auto issue_qk = [&](int t, uint32_t kslot) {
-        const uint32_t qlo = smem_desc_lo(smem_u32(sQ + t * C::kQTileBytes), 16);
+      auto issue_qk = [&](uint32_t kslot) {
         const uint32_t klo = smem_desc_lo(smem_u32(sSlot + kslot * C::kSlotBytes), 16);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss_lh(tmem + t * kBlockN, qlo + off, kDescHi, klo + off, kDescHi, idesc_qk, kk > 0 ? 1u : 0u);
+          mma_ss_lh(d_s, qlo + off, kDescHi, klo + off, kDescHi, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar_s[t]);
       };
-      // PV of tile t; the first PV of a work tile overwrites O_t, so it waits until the
-      // previous work tile's epilogue has read O_t
-      auto issue_pv = [&](int t, uint32_t vslot, bool first) -> bool {
+      // The first PV of a work tile overwrites O_t: it waits until the previous work
+      // tile's epilogue has read O_t.
+      auto issue_pv = [&](uint32_t vslot, bool first) -> bool {
         if (first) {
-          if (pvw[t] > 0) {
-            if (!wait_bounded(&bar_ofree[t], (pvw[t] - 1) & 1, cta_abort, p.status, limit, 12)) return false;
+          if (pvw > 0) {
+            if (!wait_bounded(&bar_ofree[t], (pvw - 1) & 1, cta_abort, p.status, limit, 12)) return false;
             tc_fence_after_sync();
           }
-          ++pvw[t];
+          ++pvw;
         }
         const uint32_t vlo = smem_desc_lo(smem_u32(sSlot + vslot * C::kSlotBytes), kChunkBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          mma_ts_lh(tmem + C::kColO + t * DV, tmem + C::col_p(t) + kk * 8, vlo + ((kk * 2048) >> 4), kDescHi,
-                    idesc_pv, (!first || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ts_lh(d_o, a_p + kk * 8, vlo + ((kk * 2048) >> 4), kDescHi, idesc_pv, (!first || kk > 0) ? 1u : 0u);
         mma_commit(&bar_o[t]);
+        return true;
+      };
+      // separate-P: PV of the previous step (if this tile used it), then release its V slot
+      // (an issuer waits for every fill it releases, used or not, so that it can never
+      // commit for a later fill of a slot before the other issuer released the earlier)
+      auto flush = [&]() -> bool {
+        if (!pend) return true;
+        if (!wait_bounded(&bar_full[pend_vslot], pend_vph, cta_abort, p.status, limit, 6)) return false;
+        if (pend_part) {
+          if (!wait_bounded(&bar_p[t], pend_k & 1, cta_abort, p.status, limit, 7)) return false;
+          tc_fence_after_sync();
+          if (!issue_pv(pend_vslot, pend_first)) return false;
+        }
+        mma_commit(&bar_empty[pend_vslot]);
+        pend = false;
         return true;
       };
 
@@ -323,81 +340,57 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           break;
         }
         tc_fence_after_sync();
-        uint32_t first_mask = (1u << kQTiles) - 1;  // Q tiles whose first PV of this work tile is still due
+        bool first = true;  // first PV of this work tile still due
         ok = for_each_step(T.itm, p, T.geo, [&](const Step& s) -> bool {
           const uint32_t kslot = cnt % C::kSlots, kph = (cnt / C::kSlots) & 1;
           ++cnt;
           const uint32_t vslot = cnt % C::kSlots, vph = (cnt / C::kSlots) & 1;
           ++cnt;
+          const bool part = (s.part >> t) & 1;
           if (!wait_bounded(&bar_full[kslot], kph, cta_abort, p.status, limit, 4)) return false;
-          if (C::kSepP && pend && !wait_bounded(&bar_full[pend_vslot], pend_vph, cta_abort, p.status, limit, 6))
-            return false;
-          tc_fence_after_sync();
-#pragma unroll
-          for (int t = 0; t < kQTiles; ++t) {
-            const bool part = (s.part >> t) & 1;
-            const bool pv_due = C::kSepP && pend && ((pend_mask >> t) & 1);
-            if (part && n[t] > 0) {
-              // separate P: S_t is free once softmax t has read it (it then arrived on bar_p,
-              // which also releases P_t(j-1) for its PV); P inside S_t: wait until the
-              // previous PV has consumed P_t
+          if (part) {
+            if (n > 0) {
+              // separate P: S_t is free once softmax t has read it (it then arrived on
+              // bar_p); P inside S_t: once the previous PV has consumed P_t
               uint64_t* b = C::kSepP ? &bar_p[t] : &bar_o[t];
-              if (!wait_bounded(b, (n[t] - 1) & 1, cta_abort, p.status, limit, 5)) return false;
-              tc_fence_after_sync();
-            } else if (pv_due) {
-              if (!wait_bounded(&bar_p[t], pend_k[t] & 1, cta_abort, p.status, limit, 7)) return false;
-              tc_fence_after_sync();
+              if (!wait_bounded(b, (n - 1) & 1, cta_abort, p.status, limit, 5)) return false;
             }
-            if (part) issue_qk(t, kslot);
-            if (pv_due && !issue_pv(t, pend_vslot, (pend_first >> t) & 1)) return false;
+            tc_fence_after_sync();
+            issue_qk(kslot);
           }
           mma_commit(&bar_empty[kslot]);
           if (C::kSepP) {
-            if (pend) mma_commit(&bar_empty[pend_vslot]);
+            if (!flush()) return false;
             pend = true;
-            pend_mask = s.part;
-            pend_first = s.part & first_mask;
-            first_mask &= ~s.part;
+            pend_part = part;
+            pend_first = part && first;
             pend_vslot = vslot;
             pend_vph = vph;
-#pragma unroll
-            for (int t = 0; t < kQTiles; ++t)
-              if ((s.part >> t) & 1) pend_k[t] = n[t]++;
+            pend_k = n;
+            if (part) {
+              first = false;
+              ++n;
+            }
           } else {
             if (!wait_bounded(&bar_full[vslot], vph, cta_abort, p.status, limit, 6)) return false;
-            tc_fence_after_sync();
-#pragma unroll
-            for (int t = 0; t < kQTiles; ++t) {
-              if (!((s.part >> t) & 1)) continue;
-              if (!wait_bounded(&bar_p[t], n[t] & 1, cta_abort, p.status, limit, 7)) return false;
+            if (part) {
+              if (!wait_bounded(&bar_p[t], n & 1, cta_abort, p.status, limit, 7)) return false;
               tc_fence_after_sync();
-              if (!issue_pv(t, vslot, (first_mask >> t) & 1)) return false;
-              first_mask &= ~(1u << t);
-              ++n[t];
+              if (!issue_pv(vslot, first)) return false;
+              first = false;
+              ++n;
             }
             mma_commit(&bar_empty[vslot]);
           }
           return true;
         });
-        // every S MMA of this work tile is issued: Q may be reloaded once they are done
+        // this issuer's S MMAs of the work tile are issued: Q may be reloaded once done
         mma_commit(bar_qempty);
       }
-      if (ok && pend) {  // PVs of the last step
-        if (wait_bounded(&bar_full[pend_vslot], pend_vph, cta_abort, p.status, limit, 6)) {
-          tc_fence_after_sync();
-#pragma unroll
-          for (int t = 0; t < kQTiles; ++t) {
-            if (!((pend_mask >> t) & 1)) continue;
-            if (!wait_bounded(&bar_p[t], pend_k[t] & 1, cta_abort, p.status, limit, 7)) break;
-            tc_fence_after_sync();
-            if (!issue_pv(t, pend_vslot, (pend_first >> t) & 1)) break;
-          }
-          mma_commit(&bar_empty[pend_vslot]);
-        }
-      }
-      // every MMA (and the arrivals its commits make) completes before teardown
-      mma_commit(bar_drain);
-      wait_final(bar_drain, 0, limit);
+      if (ok) flush();
+      // every MMA of this issuer (and the arrivals its commits make) completes before teardown
+      mma_commit(&bar_drain[t]);
+      wait_final(&bar_drain[t], 0, limit);
     }
   } else if (warp < kTmaWarp) {
     // ================================================================ softmax + epilogue
