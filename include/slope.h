@@ -148,6 +148,37 @@ SLOPE_API slope_status slope_cp_prefill(const slope_tensor* q, const slope_tenso
                               float scale, slope_tensor* out, slope_tensor* lse, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/*
+ * slope_cp_prefill for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this call; it exists for users of this library.
+ *
+ * Some callers cannot call cudaMalloc: code that runs inside a fixed memory
+ * budget reserved up front (a serving process whose device memory is all
+ * handed to its own pools), or code on a latency-critical path where an
+ * allocation would synchronise the device.  This variant takes no workspace:
+ * the fp32 partials live in a fixed scratch array of 64 MiB (67108864 bytes)
+ * that the library holds on every GPU that loads it, until the process exits.
+ *
+ * Same arguments and results as slope_cp_prefill, without workspace and
+ * workspace_bytes.  A request whose partials need more than 64 MiB (see
+ * slope_cp_prefill_workspace_size) returns SLOPE_ERR_WORKSPACE, before any
+ * launch, with the sizes in slope_last_error().  The call allocates nothing
+ * and calls no allocating routine.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (with that device current) and keeps it; make that first call before any
+ * stream capture.  Every call on a device shares the one array and it keeps
+ * the last call's contents (nothing in it needs to start at zero: each call
+ * writes every partial the merge reads).  Calls whose work overlaps on the
+ * GPU (for example on two streams) race on the array and give wrong results;
+ * order them on one stream or with events.
+ */
+SLOPE_API slope_status slope_cp_prefill_static_scratch(const slope_tensor* q, const slope_tensor* k,
+                                                       const slope_tensor* v, int n_chunks, slope_layout layout,
+                                                       const int64_t* chunk_sizes, int causal, int64_t window,
+                                                       float scale, slope_tensor* out, slope_tensor* lse,
+                                                       void* stream);
+
 /* Workspace bytes slope_cp_prefill needs for these sizes (0 on invalid arguments). */
 SLOPE_API size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t dv, int n_chunks, slope_layout layout,
                                        const int64_t* chunk_sizes);

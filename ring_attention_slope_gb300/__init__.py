@@ -24,6 +24,7 @@ from ._build import LIB_PATH
 __all__ = [
     "SlopeError", "load", "build", "attn_partial", "lse_merge", "cp_prefill", "cp_prefill_timed",
     "cp_prefill_workspace_size", "cp_prefill_plan", "device_status", "timeout_selftest", "LAYOUTS", "version",
+    "cp_prefill_static_scratch",
 ]
 
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "chunked": 2}
@@ -45,7 +46,7 @@ class SlopeError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
         detail = ""
-        if status == -6:
+        if status in (-6, -9):
             detail = " [" + load().slope_last_error().decode() + "]"
         super().__init__(f"{what}: {status_string(status)} ({status}){detail}")
 
@@ -54,7 +55,8 @@ _lib = None
 
 EXPORTED = ["slope_attn_partial", "slope_lse_merge", "slope_cp_prefill", "slope_cp_prefill_workspace_size",
             "slope_cp_prefill_timed", "slope_cp_prefill_plan", "slope_device_status",
-            "slope_debug_timeout_selftest", "slope_status_string", "slope_version", "slope_last_error"]
+            "slope_debug_timeout_selftest", "slope_status_string", "slope_version", "slope_last_error",
+            "slope_cp_prefill_static_scratch"]
 
 
 def build(force: bool = False) -> str:
@@ -98,6 +100,8 @@ def load():
     lib.slope_version.restype = ctypes.c_char_p
     lib.slope_last_error.argtypes = []
     lib.slope_last_error.restype = ctypes.c_char_p
+    lib.slope_cp_prefill_static_scratch.argtypes = [T, T, T, c_int, c_int, P(i64), c_int, i64, f32, T, T, vp]
+    lib.slope_cp_prefill_static_scratch.restype = c_int
     _lib = lib
     return lib
 
@@ -245,6 +249,32 @@ def cp_prefill(q, k, v, n_chunks, layout="zigzag", *, chunk_sizes=None, causal=T
                                  ctypes.byref(do), ctypes.byref(dl) if dl is not None else None,
                                  ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
     _check(st, "slope_cp_prefill")
+    return out, lse
+
+
+def cp_prefill_static_scratch(q, k, v, n_chunks, layout="zigzag", *, chunk_sizes=None, causal=True, window=0,
+                              scale=0.0, out=None, lse=None, out_dtype=None, want_lse=True, stream=None):
+    """cp_prefill for callers that cannot allocate device memory.
+
+    The partials live in the library's fixed 64 MiB scratch array instead of a
+    caller workspace; larger requests raise SlopeError (SLOPE_ERR_WORKSPACE).
+    Calls that overlap on the GPU share that array and race.  Returns ``(out, lse)``.
+    """
+    torch = _torch()
+    S, Hq, _ = q.shape
+    dv = v.shape[2]
+    if out is None:
+        out = torch.empty((S, Hq, dv), dtype=out_dtype or torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, S), dtype=torch.float32, device=q.device)
+    arr, ptr = _chunk_array(chunk_sizes)
+    dq, dk, dvv, do = _desc(q), _desc(k), _desc(v), _desc(out)
+    dl = _desc(lse) if lse is not None else None
+    st = load().slope_cp_prefill_static_scratch(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dvv),
+                                                int(n_chunks), _layout(layout), ptr, int(bool(causal)),
+                                                int(window), float(scale), ctypes.byref(do),
+                                                ctypes.byref(dl) if dl is not None else None, _stream_ptr(stream))
+    _check(st, "slope_cp_prefill_static_scratch")
     return out, lse
 
 

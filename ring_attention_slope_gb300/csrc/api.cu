@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -418,6 +419,37 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   return SLOPE_OK;
 }
 
+// ---------------------------------------------------------------- fixed scratch (no allocation)
+
+// Partials of slope_cp_prefill_static_scratch: one array per device that loads the library.
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+std::atomic<void*> g_static_scratch_ptr[64];
+
+// Device address of the scratch array for the current device, looked up once per device.
+void* static_scratch_ptr() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cuda_fail("cudaGetDevice", e);
+    return nullptr;
+  }
+  if (dev < 0 || dev >= 64) {
+    cuda_fail("fixed scratch: device index out of range");
+    return nullptr;
+  }
+  void* ptr = g_static_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (ptr == nullptr) {
+    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess || ptr == nullptr) {
+      cuda_fail("cudaGetSymbolAddress(fixed scratch)", e);
+      return nullptr;
+    }
+    g_static_scratch_ptr[dev].store(ptr, std::memory_order_release);
+  }
+  return ptr;
+}
+
 }  // namespace
 
 // ==================================================================== exported
@@ -546,6 +578,26 @@ slope_status slope_cp_prefill(const slope_tensor* q, const slope_tensor* k, cons
                               size_t workspace_bytes, void* stream) {
   return cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, out, lse, workspace,
                          workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+slope_status slope_cp_prefill_static_scratch(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v,
+                                             int n_chunks, slope_layout layout, const int64_t* chunk_sizes,
+                                             int causal, int64_t window, float scale, slope_tensor* out,
+                                             slope_tensor* lse, void* stream) {
+  if (q == nullptr || v == nullptr) return SLOPE_ERR_NULL;
+  if (q->ndim != 3 || v->ndim != 3) return SLOPE_ERR_SHAPE;
+  const size_t need = slope_cp_prefill_workspace_size(q->shape[0], q->shape[1], v->shape[2], n_chunks, layout,
+                                                      chunk_sizes);
+  if (need > kStaticScratchBytes) {
+    std::snprintf(g_last_error, sizeof(g_last_error),
+                  "fixed scratch holds %zu bytes; this request needs %zu (use slope_cp_prefill with a workspace)",
+                  kStaticScratchBytes, need);
+    return SLOPE_ERR_WORKSPACE;
+  }
+  void* scratch = static_scratch_ptr();
+  if (scratch == nullptr) return SLOPE_ERR_CUDA;
+  return slope_cp_prefill(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, out, lse, scratch,
+                          kStaticScratchBytes, stream);
 }
 
 slope_status slope_cp_prefill_timed(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v,
