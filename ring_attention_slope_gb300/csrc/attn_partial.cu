@@ -53,7 +53,7 @@ struct K1Cfg {
   static constexpr int kVTileBytes = kVChunks * kChunkBytes;
   static constexpr int kSlotBytes = kKTileBytes > kVTileBytes ? kKTileBytes : kVTileBytes;
   static constexpr int kSlots = DQK == 64 ? 8 : (DQK == 128 ? 4 : 2);
-  static constexpr int kNumBars = 1 + 2 * kSlots + 5 * kQTiles + 1;
+  static constexpr int kNumBars = 1 + 2 * kSlots + 6 * kQTiles + 1;
   static constexpr int kBarOffset = kQTiles * kQTileBytes + kSlots * kSlotBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 8 * kNumBars + 16;
   static constexpr uint32_t kColO = 256;
@@ -170,7 +170,8 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   uint64_t* bar_ofree = bar_o + kQTiles;
   uint64_t* bar_qempty = bar_ofree + kQTiles;
   uint64_t* bar_drain = bar_qempty + 1;  // one per MMA issuer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + kQTiles);
+  uint64_t* bar_sfree = bar_drain + kQTiles;  // softmax t has loaded S_t into registers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_sfree + kQTiles);
   volatile int* cta_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -198,7 +199,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       mbar_init(&bar_ofree[t], 4);
     }
     mbar_init(bar_qempty, kQTiles);
-    for (int t = 0; t < kQTiles; ++t) mbar_init(&bar_drain[t], 1);
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(&bar_drain[t], 1);
+      mbar_init(&bar_sfree[t], 4);  // one arrival per softmax warp
+    }
     fence_barrier_init();
   }
   if (threadIdx.x == kTmaWarp * 32) {
@@ -350,9 +354,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           if (!wait_bounded(&bar_full[kslot], kph, cta_abort, p.status, limit, 4)) return false;
           if (part) {
             if (n > 0) {
-              // separate P: S_t is free once softmax t has read it (it then arrived on
-              // bar_p); P inside S_t: once the previous PV has consumed P_t
-              uint64_t* b = C::kSepP ? &bar_p[t] : &bar_o[t];
+              // separate P: S_t is free as soon as softmax t has loaded it into registers
+              // (bar_sfree), so S_t(j) overlaps softmax t's work on step j-1; P inside
+              // S_t: once the previous PV has consumed P_t
+              uint64_t* b = C::kSepP ? &bar_sfree[t] : &bar_o[t];
               if (!wait_bounded(b, (n - 1) & 1, cta_abort, p.status, limit, 5)) return false;
             }
             tc_fence_after_sync();
@@ -427,6 +432,11 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         reg_fence(r1);
         reg_fence(r2);
         reg_fence(r3);
+        if (C::kSepP) {  // S_t is in registers: the next S MMA of this tile may overwrite it
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_sfree[t]);
+        }
         float sv[128];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
