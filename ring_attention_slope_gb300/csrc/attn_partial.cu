@@ -476,20 +476,14 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
         // p = exp2(s * sl2 - m), packed to bf16 pairs; row sum in fp32 (four packed chains)
-        const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-msub, -msub);
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                         make_float2(0.f, 0.f)};
+        const uint64_t sl2v = pack_f32x2(sl2, sl2), negm = pack_f32x2(-msub, -msub);
+        uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float2 x = ffma2(make_float2(sv[2 * i], sv[2 * i + 1]), sl2v, negm);
-          const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-          acc[i & 3] = fadd2(acc[i & 3], make_float2(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        const float2 acc01 = fadd2(acc[0], acc[1]), acc23 = fadd2(acc[2], acc[3]);
-        const float2 accs = fadd2(acc01, acc23);
-        l += accs.x + accs.y;
+        for (int i = 0; i < 64; ++i) pk[i] = softmax_pair(sv[2 * i], sv[2 * i + 1], sl2v, negm, acc[i & 3]);
+        const float2 c0 = unpack_f32x2(acc[0]), c1 = unpack_f32x2(acc[1]);
+        const float2 c2 = unpack_f32x2(acc[2]), c3 = unpack_f32x2(acc[3]);
+        l += ((c0.x + c0.y) + (c1.x + c1.y)) + ((c2.x + c2.y) + (c3.x + c3.y));
         if (!C::kSepP) {  // P over S_t: every S value is already in registers
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * c]));

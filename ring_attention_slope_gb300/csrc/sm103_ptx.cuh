@@ -321,6 +321,36 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   asm("mov.b64 {%0,%1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
   return r;
 }
+// One pair of softmax elements: x = s * sl2 - m (packed FMA), p = 2^x (two MUFU ops),
+// acc += p (packed add, accumulator kept as a 64-bit register pair), and p packed to
+// bf16x2 (round to nearest even).  sl2_m holds {sl2, sl2} and neg_m {-m, -m}.
+__device__ __forceinline__ uint32_t softmax_pair(float s0, float s1, uint64_t sl2_pair, uint64_t negm_pair,
+                                                 uint64_t& acc) {
+  uint32_t packed;
+  asm("{\n\t.reg .b64 sp, xp, pp;\n\t.reg .f32 x0, x1, p0, p1;\n\t"
+      "mov.b64 sp, {%2, %3};\n\t"
+      "fma.rn.f32x2 xp, sp, %4, %5;\n\t"
+      "mov.b64 {x0, x1}, xp;\n\t"
+      "ex2.approx.ftz.f32 p0, x0;\n\t"
+      "ex2.approx.ftz.f32 p1, x1;\n\t"
+      "mov.b64 pp, {p0, p1};\n\t"
+      "add.rn.f32x2 %1, %1, pp;\n\t"
+      "cvt.rn.bf16x2.f32 %0, p1, p0;\n\t}"
+      : "=r"(packed), "+l"(acc)
+      : "f"(s0), "f"(s1), "l"(sl2_pair), "l"(negm_pair));
+  return packed;
+}
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
