@@ -42,6 +42,16 @@ constexpr int kMmaWarp = kTmaWarp + 1;
 // a thread at 168 registers.
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
+// Of every 16 element pairs of a score row, this many take 2^x on the FMA pipe
+// (softmax_pair_poly) and the rest on the MUFU unit, which bounds the softmax: with two
+// softmax warps per SM sub-partition, 2 ex2 cost 8 MUFU cycles and the polynomial pair
+// about 14 more FMA-pipe cycles and 8 more issue slots than the MUFU pair.  Measured on
+// the causal 32K zigzag workload (kernel TFLOP/s): 0 -> 745, 1 -> 749, 2 -> 765,
+// 3 -> 696, 4 -> 685 (beyond 2 the register spills and the issue slots win).  A masked
+// score (-inf) gives 2^-125 there instead of 0: once a row has seen a key its sum l is
+// >= 1 and the term is far below bf16 resolution; before that the row's max is -inf
+// and the first visible key rescales l and O by 0; a row that never sees a key writes 0.
+constexpr int kPolyPairsPer16 = 2;
 
 template <int DQK, int DV>
 struct K1Cfg {
@@ -479,8 +489,12 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         const uint64_t sl2v = pack_f32x2(sl2, sl2), negm = pack_f32x2(-msub, -msub);
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[64];
+        const Exp2Poly poly = exp2_poly_consts();
 #pragma unroll
-        for (int i = 0; i < 64; ++i) pk[i] = softmax_pair(sv[2 * i], sv[2 * i + 1], sl2v, negm, acc[i & 3]);
+        for (int i = 0; i < 64; ++i)
+          pk[i] = (i & 15) < kPolyPairsPer16
+                      ? softmax_pair_poly(sv[2 * i], sv[2 * i + 1], sl2v, negm, acc[i & 3], poly)
+                      : softmax_pair(sv[2 * i], sv[2 * i + 1], sl2v, negm, acc[i & 3]);
         const float2 c0 = unpack_f32x2(acc[0]), c1 = unpack_f32x2(acc[1]);
         const float2 c2 = unpack_f32x2(acc[2]), c3 = unpack_f32x2(acc[3]);
         l += ((c0.x + c0.y) + (c1.x + c1.y)) + ((c2.x + c2.y) + (c3.x + c3.y));
@@ -528,7 +542,9 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                   static_cast<int64_t>(T.h) * p.out_shead;
       if (nl > 0) {
         tc_fence_after_sync();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        // a row that saw no key keeps m = -inf; its l holds only the clamped 2^-125
+        // terms of the polynomial pairs, and its output is 0
+        const float inv = (l > 0.f && m_used > -INFINITY) ? 1.f / l : 0.f;
 #pragma unroll
         for (int c = 0; c < DV / 32; ++c) {
           uint32_t o[32];

@@ -340,6 +340,64 @@ __device__ __forceinline__ uint32_t softmax_pair(float s0, float s1, uint64_t sl
       : "f"(s0), "f"(s1), "l"(sl2_pair), "l"(negm_pair));
   return packed;
 }
+// The same pair with 2^x on the FMA pipe instead of the MUFU unit, so that the kernel can
+// move part of its exponentials off the MUFU unit, which bounds the softmax.  2^x is
+// reduced Cody-Waite style to 2^n * 2^f: adding 1.5 * 2^23 rounds x to the integer n
+// (left in the low mantissa bits of t), f = x - n lies in [-1/2, 1/2], 2^f is a cubic
+// 1 + c1 f + c2 f^2 + c3 f^3 fitted for the smallest maximum relative error
+// (exp2_poly_fit.py beside this file: 1.0e-4 in float32, far below the 2^-9 of the
+// bf16 rounding that follows; c0 = 1, so an integer x gives 2^x exactly), and 2^n is
+// added into the exponent field (t << 23 keeps n << 23 exactly, because every set bit
+// of 1.5 * 2^23 lies at bit 22 or above).  x is clamped to >= -125 first, so the
+// exponent cannot underflow: 2^x for x < -125 (and -inf) comes out as about 2^-125,
+// not 0, and a NaN x as 2^-125 too.
+// poly holds {c3, c2, c1, c0} as {c, c} pairs; magic is {1.5 * 2^23, 1.5 * 2^23}.
+struct Exp2Poly {
+  uint64_t magic, c3, c2, c1, c0;
+};
+__device__ __forceinline__ uint32_t softmax_pair_poly(float s0, float s1, uint64_t sl2_pair, uint64_t negm_pair,
+                                                      uint64_t& acc, const Exp2Poly& k) {
+  uint32_t packed;
+  asm("{\n\t.reg .b64 sp, xp, tp, jp, fp, qp, pp;\n\t.reg .f32 x0, x1, p0, p1;\n\t"
+      ".reg .b32 t0, t1, q0, q1, e0, e1;\n\t"
+      "mov.b64 sp, {%2, %3};\n\t"
+      "fma.rn.f32x2 xp, sp, %4, %5;\n\t"
+      "mov.b64 {x0, x1}, xp;\n\t"
+      "max.f32 x0, x0, 0fC2FA0000;\n\t"
+      "max.f32 x1, x1, 0fC2FA0000;\n\t"
+      "mov.b64 xp, {x0, x1};\n\t"
+      "add.rn.f32x2 tp, xp, %6;\n\t"
+      "sub.rn.f32x2 jp, tp, %6;\n\t"
+      "sub.rn.f32x2 fp, xp, jp;\n\t"
+      "fma.rn.f32x2 qp, %7, fp, %8;\n\t"
+      "fma.rn.f32x2 qp, qp, fp, %9;\n\t"
+      "fma.rn.f32x2 qp, qp, fp, %10;\n\t"
+      "mov.b64 {t0, t1}, tp;\n\t"
+      "mov.b64 {q0, q1}, qp;\n\t"
+      "shl.b32 e0, t0, 23;\n\t"
+      "shl.b32 e1, t1, 23;\n\t"
+      "add.u32 e0, e0, q0;\n\t"
+      "add.u32 e1, e1, q1;\n\t"
+      "mov.b32 p0, e0;\n\t"
+      "mov.b32 p1, e1;\n\t"
+      "mov.b64 pp, {p0, p1};\n\t"
+      "add.rn.f32x2 %1, %1, pp;\n\t"
+      "cvt.rn.bf16x2.f32 %0, p1, p0;\n\t}"
+      : "=r"(packed), "+l"(acc)
+      : "f"(s0), "f"(s1), "l"(sl2_pair), "l"(negm_pair), "l"(k.magic), "l"(k.c3), "l"(k.c2), "l"(k.c1), "l"(k.c0));
+  return packed;
+}
+// Coefficients printed by exp2_poly_fit.py (float32 bit patterns).
+constexpr uint32_t kExp2PolyC0 = 0x3F800000u;  // exactly 1: integer x gives 2^x exactly
+constexpr uint32_t kExp2PolyC1 = 0x3F317AFDu;
+constexpr uint32_t kExp2PolyC2 = 0x3E780626u;
+constexpr uint32_t kExp2PolyC3 = 0x3D61510Bu;
+constexpr uint32_t kExp2PolyMagic = 0x4B400000u;  // 1.5 * 2^23
+__host__ __device__ constexpr uint64_t splat_bits(uint32_t b) { return (static_cast<uint64_t>(b) << 32) | b; }
+__device__ __forceinline__ Exp2Poly exp2_poly_consts() {
+  return {splat_bits(kExp2PolyMagic), splat_bits(kExp2PolyC3), splat_bits(kExp2PolyC2), splat_bits(kExp2PolyC1),
+          splat_bits(kExp2PolyC0)};
+}
 __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
