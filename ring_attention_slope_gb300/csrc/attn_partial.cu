@@ -133,6 +133,33 @@ __device__ __forceinline__ bool for_each_step(const WorkItem& it, const AttnPara
   return true;
 }
 
+// The K/V tiles of one key range that a single Q tile (rows at positions qa..qb)
+// sees: j in [lo, hi], and among them the ones it sees in full (no masked key): j in
+// [flo, fhi].  Step for step these are the tiles of for_each_step whose part bit for
+// that Q tile is set, with its full bit; the softmax warps walk them directly, which
+// keeps their per-step loop state to a few registers.
+struct TileRange {
+  int kpos0, len, lo, hi, flo, fhi;
+};
+__device__ __forceinline__ TileRange tile_range(int row0, int len, int qa, int qb, const AttnParams& p) {
+  TileRange R;
+  R.kpos0 = p.kv_pos_off + row0;
+  R.len = len;
+  const int last = (len + kBlockN - 1) / kBlockN - 1;
+  R.hi = p.causal ? min(last, floor_div(qb - R.kpos0, kBlockN)) : last;
+  R.lo = 0;
+  if (p.window > 0) {
+    R.lo = max(0, floor_div(qa - p.window + 1 - R.kpos0, kBlockN));
+    // a short last tile: its own last key decides
+    if (R.lo == last && qa - (R.kpos0 + len - 1) >= p.window) R.lo = last + 1;
+  }
+  R.fhi = (len % kBlockN == 0) ? last : last - 1;
+  if (p.causal) R.fhi = min(R.fhi, floor_div(qa - R.kpos0 - (kBlockN - 1), kBlockN));
+  R.flo = R.lo;
+  if (p.window > 0) R.flo = max(R.flo, floor_div(qb - R.kpos0 - p.window, kBlockN) + 1);
+  return R;
+}
+
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
 // One unit of work: an item's 256-row block for one query head.
@@ -428,8 +455,9 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       float m_used = -INFINITY;  // running max in log2-scaled units
       float l = 0.f;             // running sum of exp2(s*sl2 - m_used)
       int nl = 0;                // steps of this work tile
-      ok = for_each_step(T.itm, p, T.geo, [&](const Step& s) -> bool {
-        if (!((s.part >> t) & 1)) return true;
+      const int qa_t = t == 0 ? T.geo.qa[0] : T.geo.qa[1];
+      const int qb_t = qa_t + rows_t - 1;
+      auto step = [&](const bool full, const int kpos, const int valid) -> bool {
         if (!warp_all(wait_bounded(&bar_s[t], n & 1, cta_abort, p.status, limit, 8))) return false;
         tc_fence_after_sync();
         uint32_t r0[32], r1[32], r2[32], r3[32];
@@ -455,11 +483,11 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           sv[64 + i] = __uint_as_float(r2[i]);
           sv[96 + i] = __uint_as_float(r3[i]);
         }
-        if (!((s.full >> t) & 1)) {
+        if (!full) {
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c) {
-            const int kp = s.kpos + c;
-            const bool vis = c < s.valid && (!p.causal || kp <= q_pos) && (p.window == 0 || q_pos - kp < p.window);
+            const int kp = kpos + c;
+            const bool vis = c < valid && (!p.causal || kp <= q_pos) && (p.window == 0 || q_pos - kp < p.window);
             if (!vis) sv[c] = -INFINITY;
           }
         }
@@ -530,7 +558,13 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         ++n;
         ++nl;
         return true;
-      });
+      };
+      for (int r = 0; r < T.itm.n_kv && ok; ++r) {
+        const TileRange R = tile_range(r == 0 ? T.itm.kv[0].row0 : T.itm.kv[1].row0,
+                                       r == 0 ? T.itm.kv[0].len : T.itm.kv[1].len, qa_t, qb_t, p);
+        for (int j = R.lo; j <= R.hi && ok; ++j)
+          ok = step(j >= R.flo && j <= R.fhi, R.kpos0 + j * kBlockN, min(kBlockN, R.len - j * kBlockN));
+      }
       if (!ok) break;
 
       // ---- epilogue: out = O / l, lse = ln(sum exp(scaled scores))
