@@ -39,7 +39,9 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "causal_gqa_s32k_zigzag8"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-K1_SOURCE = os.path.join(ROOT, "ring_attention_slope_gb300", "csrc", "attn_partial.cu")
+# every source file the attention kernel is compiled from (its ncu summary is valid for this hash only)
+K1_SOURCES = [os.path.join(ROOT, "ring_attention_slope_gb300", "csrc", f)
+              for f in ("attn_partial.cu", "sm103_ptx.cuh", "kernels.cuh", "waits.cuh")]
 
 
 # ---------------------------------------------------------------- helpers
@@ -55,8 +57,11 @@ def load_peaks():
 
 
 def k1_source_hash():
-    with open(K1_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in K1_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload_name):
