@@ -307,11 +307,7 @@ def run_gpu(args, w):
     tokens_s = w.S * args.steps * world / (elapsed_ms * 1e-3)
     peaks, peak_src = load_peaks()
     k1_tflops = flops_step * args.steps / (k1_ms * 1e-3) / 1e12
-    n_planes = n if w.layout != "chunked" else 2
-    # merge: algorithmic bytes = every live partial read once + final out/lse written
-    live_fraction = merge_live_fraction(w, n)
-    merge_bytes = (w.S * w.Hq * (w.dv * 4 + 4) * n_planes * live_fraction + w.S * w.Hq * 4 * n_planes * (1 - live_fraction)
-                   + w.S * w.Hq * (w.dv * 2 + 4))
+    merge_bytes = merge_bytes_per_launch(slope, w, n, sizes, window)
     k2_gbs = merge_bytes * k2_n / (k2_ms * 1e-3) / 1e9 if k2_ms > 0 else None
 
     # ---- end to end through the public call with pinned host buffers
@@ -354,15 +350,32 @@ def run_gpu(args, w):
     return 0
 
 
-def merge_live_fraction(w, n):
-    """Fraction of (row, plane) partials that hold a visible key (the merge reads only those)."""
-    if w.layout == "chunked":
-        sizes = wl.chunk_sizes(w)
-        return 1.0 - sizes[0] / w.S / 2.0  # chunk 0 has no prefix partial
-    if w.layout == "zigzag":
-        # early sub-chunk r sees r + 1 of the N steps, late sub-chunks see all N
-        return (sum(r + 1 for r in range(n)) + n * n) / (2 * n * n)
-    return (n + 1) / (2 * n)
+def merge_bytes_per_launch(slope, w, n, sizes, window):
+    """Algorithmic DRAM bytes of one merge launch, exact, from the launch plan.
+
+    The merge reads, for every row and head, the lse of each merged plane and the fp32
+    partial output of the planes in which that row saw at least one key, and writes the
+    bf16 output and fp32 lse.  A plane none of whose rows sees a key is not merged.  In
+    the ring and chunked layouts a row's position is its row index, so a row of a plan
+    item is live when one of the item's key ranges, cut to the causal limit (key <= row)
+    and the window (row - key < window), is not empty.
+    """
+    items, _, n_planes = slope.cp_prefill_plan(w.S, n, w.layout, chunk_sizes=sizes, causal=True, window=window)
+    live_rows = np.zeros(n_planes, dtype=np.int64)
+    plane_live = np.zeros(n_planes, dtype=bool)
+    plane_live[0] = True
+    for it in items:
+        if it["kv"]:
+            plane_live[it["plane"]] = True
+        q = np.arange(it["q_row0"], it["q_row0"] + it["q_len"], dtype=np.int64)
+        seen = np.zeros(q.shape, dtype=bool)
+        for k0, ln in it["kv"]:
+            lo = np.maximum(k0, q - window + 1) if window > 0 else np.full(q.shape, k0)
+            hi = np.minimum(k0 + ln - 1, q)
+            seen |= lo <= hi
+        live_rows[it["plane"]] += int(seen.sum())
+    reads = int(plane_live.sum()) * w.S * 4 + int(live_rows[plane_live].sum()) * w.dv * 4
+    return float(w.Hq * (reads + w.S * (w.dv * 2 + 4)))
 
 
 def run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier, dist):

@@ -131,7 +131,9 @@ SLOPE_API slope_status slope_lse_merge(const slope_tensor* outs, const slope_ten
  *     simulated ranks.  At ring step t rank r holds the keys/values of rank
  *     (r - t) mod n_chunks; each step is ONE attention-kernel launch covering
  *     every rank, writing one partial per (rank, step); a final merge launch
- *     combines each row's partials.  CONTIGUOUS needs S % n_chunks == 0,
+ *     combines each row's partials.  A step in which no query sees any key
+ *     (possible only with a window) is skipped, and so is its partial in the
+ *     merge.  CONTIGUOUS needs S % n_chunks == 0,
  *     ZIGZAG needs S % (2*n_chunks) == 0.  1 <= n_chunks <= 32.
  *   layout SLOPE_LAYOUT_CHUNKED: n_chunks query chunks, sizes chunk_sizes[0..n)
  *     (summing to S), or NULL for ceil(S/n_chunks) with a shorter last chunk.
@@ -202,7 +204,9 @@ SLOPE_API slope_status slope_cp_prefill_timed(const slope_tensor* q, const slope
  * Host-only view of the work decomposition slope_cp_prefill performs (no GPU
  * needed).  One entry per (launch, query block): the query rows, the partial
  * plane written and the key/value row ranges attended in that launch
- * (after dropping blocks the mask hides entirely).
+ * (after dropping blocks the mask hides entirely).  An entry with n_kv = 0
+ * stands for rows whose partial is empty; a plane whose entries all have
+ * n_kv = 0 is neither launched nor merged (plane 0 always is).
  */
 typedef struct {
   int32_t launch;     /* attention launch index (ring step or chunk)      */

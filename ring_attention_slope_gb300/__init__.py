@@ -288,6 +288,9 @@ def cp_prefill_timed(q, k, v, n_chunks, layout, events, *, chunk_sizes=None, cau
     arr, ptr = _chunk_array(chunk_sizes)
     handles = []
     for a, b in events:
+        for e in (a, b):
+            if e.cuda_event == 0:  # torch creates the CUDA event lazily, at its first record
+                e.record()
         handles += [a.cuda_event, b.cuda_event]
     ev = (ctypes.c_void_p * len(handles))(*handles)
     kinds = (ctypes.c_int * len(events))()

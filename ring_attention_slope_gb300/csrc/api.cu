@@ -379,12 +379,23 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   base.status = status;
   base.wait_limit_ns = wait_limit_ns();
 
+  // A plane none of whose items sees a key (ring steps that a sliding window leaves
+  // empty) is neither computed nor merged: its partials would all be out = 0 and
+  // lse = -inf, which the merge ignores.  Plane 0 is always kept, so that the merge
+  // writes -inf / 0 for rows that see nothing at all.
+  std::vector<char> plane_live(static_cast<size_t>(plan.n_planes), 0);
+  plane_live[0] = 1;
+  for (const PItem& it : plan.items)
+    if (it.n_kv > 0) plane_live[static_cast<size_t>(it.plane)] = 1;
+
   // One or more launches per ring step / chunk, in order.
   size_t i = 0;
   std::vector<std::vector<WorkItem>> groups;
   for (int l = 0; l < plan.n_launches; ++l) {
     std::vector<PItem> items;
-    while (i < plan.items.size() && plan.items[i].launch == l) items.push_back(plan.items[i++]);
+    for (; i < plan.items.size() && plan.items[i].launch == l; ++i)
+      if (plane_live[static_cast<size_t>(plan.items[i].plane)]) items.push_back(plan.items[i]);
+    if (items.empty()) continue;
     pack_items(items, causal, groups);
     for (const auto& g : groups)
       if ((st = run_attention(g, static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, base, tm, stream)) !=
@@ -393,17 +404,19 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   }
 
   MergeParams mp{};
-  mp.n = plan.n_planes;
+  mp.n = 0;
   mp.H = static_cast<int32_t>(Hq);
   mp.dv = static_cast<int32_t>(dv);
   mp.S = S;
   for (int pl = 0; pl < plan.n_planes; ++pl) {
-    mp.outs[pl] = planes + static_cast<int64_t>(pl) * S * Hq * dv;
-    mp.lses[pl] = lse_planes + static_cast<int64_t>(pl) * S * Hq;
-    mp.o_srow[pl] = Hq * dv;
-    mp.o_shead[pl] = dv;
-    mp.l_srow[pl] = Hq;
-    mp.l_shead[pl] = 1;
+    if (!plane_live[static_cast<size_t>(pl)]) continue;
+    const int m = mp.n++;
+    mp.outs[m] = planes + static_cast<int64_t>(pl) * S * Hq * dv;
+    mp.lses[m] = lse_planes + static_cast<int64_t>(pl) * S * Hq;
+    mp.o_srow[m] = Hq * dv;
+    mp.o_shead[m] = dv;
+    mp.l_srow[m] = Hq;
+    mp.l_shead[m] = 1;
   }
   mp.out = out->data;
   mp.out_bf16 = out->dtype == SLOPE_BF16 ? 1 : 0;

@@ -160,6 +160,19 @@ __device__ __forceinline__ TileRange tile_range(int row0, int len, int qa, int q
   return R;
 }
 
+// True if at least one Q tile of the work tile sees at least one key.  Work tiles
+// without any (for example ring steps that a sliding window leaves empty) only need
+// their -inf log-sum-exp written by the softmax warps: the TMA and MMA warps skip them,
+// Q load and all, and count only the others in their Q-buffer phases.
+__device__ __forceinline__ bool has_steps(const WorkItem& it, const AttnParams& p, const TileGeom& g) {
+  bool any = false;
+  for_each_step(it, p, g, [&](const Step&) -> bool {
+    any = true;
+    return false;
+  });
+  return any;
+}
+
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
 // One unit of work: an item's 256-row block for one query head.
@@ -262,6 +275,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       for (int w = blockIdx.x; w < total; w += gridDim.x) {
         Tile T;
         decode_tile(p, w, T);
+        if (!has_steps(T.itm, p, T.geo)) continue;
         // Q of the previous work tile is in use until its last S MMAs are done
         if (wt > 0 && !wait_bounded(bar_qempty, (wt - 1) & 1, cta_abort, p.status, limit, 11)) {
           ok = false;
@@ -373,13 +387,15 @@ __global__ void __launch_bounds__(kK1Threads, 1)
 
       bool ok = true;
       int wt = 0;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++wt) {
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         Tile T;
         decode_tile(p, w, T);
+        if (!has_steps(T.itm, p, T.geo)) continue;
         if (!wait_bounded(bar_q, wt & 1, cta_abort, p.status, limit, 3)) {
           ok = false;
           break;
         }
+        ++wt;
         tc_fence_after_sync();
         bool first = true;  // first PV of this work tile still due
         ok = for_each_step(T.itm, p, T.geo, [&](const Step& s) -> bool {

@@ -187,6 +187,22 @@ def test_cp_prefill_tiny_all_layouts(layout, n, window):
     assert slope.device_status() == (0, 0)
 
 
+def test_cp_prefill_skips_ring_steps_without_keys():
+    """With a window shorter than a sub-chunk, zigzag ring steps 2..N-2 see no key: no launch, no merge input."""
+    S, Hq, Hkv, d, N, W = 2048, 4, 2, 64, 8, 100
+    q, k, v = qkv(S, Hq, Hkv, d, d, seed=17)
+    items, n_steps, _ = slope.cp_prefill_plan(S, N, "zigzag", window=W)
+    live = {it["plane"] for it in items if it["kv"]} | {0}
+    assert live == {0, 1, N - 1}
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_steps + 1)]
+    out, lse, n_launches, kinds = slope.cp_prefill_timed(q, k, v, N, "zigzag", events, window=W)
+    torch.cuda.synchronize()
+    assert kinds.count(0) == len(live) and kinds.count(1) == 1 and n_launches == len(live) + 1
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, window=W)
+    compare(out.float().cpu(), lse.cpu(), ro, rl, "zigzag-8 window 100")
+    assert slope.device_status() == (0, 0)
+
+
 def test_cp_prefill_chunked_ragged_sizes_and_fp32_out():
     S, Hq, Hkv, d = 1000, 4, 2, 64
     q, k, v = qkv(S, Hq, Hkv, d, d, seed=21, scale_v=0.8)
