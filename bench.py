@@ -330,7 +330,9 @@ def run_gpu(args, w):
                      "unit": "TFLOP/s", "frac": k1_tflops / peaks["bf16_tflops_sustained"],
                      "traffic": profiled_traffic(w.name), "kernel": "attn_partial_kernel",
                      "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a multi-launch step)",
-                     "launches": k1_n, "avg_launch_ms": k1_ms / max(1, k1_n)},
+                     "launches": k1_n, "avg_launch_ms": k1_ms / max(1, k1_n),
+                     # one exponential per visible (query, key) pair and query head
+                     "exp_per_s": flops_step / (2.0 * (w.dqk + w.dv)) * args.steps / (k1_ms * 1e-3)},
         "roofline_merge": {"bound": "hbm", "achieved": k2_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": (k2_gbs / peaks["hbm_gbs"]) if k2_gbs else None,
                            "bytes_per_launch": merge_bytes, "kernel": "lse_merge_kernel",
