@@ -123,6 +123,23 @@ bool make_map(CUtensorMap* m, const slope_tensor* t) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view {dv, H, rows} of an fp32 output with row/head strides in elements; box = 32
+// columns x 1 head x 32 rows (one softmax warp's rows), 128-byte swizzle, written by TMA
+// stores from the attention kernel's epilogue.  Returns false if the map cannot be built
+// (the kernel then stores directly).
+bool make_out_map(CUtensorMap* m, float* base, int64_t rows, int64_t H, int64_t dv, int64_t srow, int64_t shead) {
+  auto enc = encode_fn();
+  if (enc == nullptr || rows <= 0 || rows > 0x7fffffffLL) return false;
+  std::memset(m, 0, sizeof(*m));
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dv), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(shead) * 4, static_cast<cuuint64_t>(srow) * 4};
+  cuuint32_t box[3] = {32, 1, 32};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- work decomposition
 
 struct Range {
@@ -305,13 +322,13 @@ cudaError_t record(Timing* tm, bool before, int kind, cudaStream_t stream) {
 }
 
 slope_status run_attention(const std::vector<WorkItem>& group, int dqk, int dv, const CUtensorMap& tq,
-                           const CUtensorMap& tk, const CUtensorMap& tv, AttnParams base, Timing* tm,
-                           cudaStream_t stream) {
+                           const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to, AttnParams base,
+                           Timing* tm, cudaStream_t stream) {
   base.n_items = static_cast<int32_t>(group.size());
   for (size_t i = 0; i < group.size(); ++i) base.items[i] = group[i];
   cudaError_t e;
   if ((e = record(tm, true, 0, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
-  if ((e = launch_attn_partial(dqk, dv, tq, tk, tv, base, stream)) != cudaSuccess)
+  if ((e = launch_attn_partial(dqk, dv, tq, tk, tv, to, base, stream)) != cudaSuccess)
     return cuda_fail("attention kernel launch", e);
   if ((e = record(tm, false, 0, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
   return SLOPE_OK;
@@ -378,6 +395,10 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   base.lse_splane = S * Hq;
   base.status = status;
   base.wait_limit_ns = wait_limit_ns();
+  CUtensorMap to;
+  base.out_plane_rows = S;
+  base.out_tma = make_out_map(&to, planes, static_cast<int64_t>(plan.n_planes) * S, Hq, dv, Hq * dv, dv) ? 1 : 0;
+  if (!base.out_tma) to = tq;  // never used
 
   // A plane none of whose items sees a key (ring steps that a sliding window leaves
   // empty) is neither computed nor merged: its partials would all be out = 0 and
@@ -398,7 +419,7 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
     if (items.empty()) continue;
     pack_items(items, causal, groups);
     for (const auto& g : groups)
-      if ((st = run_attention(g, static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, base, tm, stream)) !=
+      if ((st = run_attention(g, static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, to, base, tm, stream)) !=
           SLOPE_OK)
         return st;
   }
@@ -535,7 +556,11 @@ slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, co
   base.lse_splane = 0;
   base.status = status;
   base.wait_limit_ns = wait_limit_ns();
-  return run_attention(groups[0], static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, base, nullptr,
+  CUtensorMap to;
+  base.out_plane_rows = 0;
+  base.out_tma = make_out_map(&to, base.out, Sq, Hq, dv, out->stride[0], out->stride[1]) ? 1 : 0;
+  if (!base.out_tma) to = tq;  // never used
+  return run_attention(groups[0], static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, to, base, nullptr,
                        static_cast<cudaStream_t>(stream));
 }
 

@@ -10,7 +10,9 @@
 //
 // Structure (one CTA = one item x 256 query rows x one query head):
 //   warps 0-3   online softmax of Q tile 0 (one query row per thread = TMEM lane),
-//   warps 4-7   online softmax of Q tile 1; each also runs its tile's epilogue.
+//   warps 4-7   online softmax of Q tile 1; each also runs its tile's epilogue,
+//               which stages O in shared memory (a 32 x 32 fp32 box per warp)
+//               and writes it with TMA stores.
 //   warp 8      TMA producer: Q tiles once, then K and V tiles through a ring
 //               of shared-memory slots (128-byte swizzle, 64-column chunks).
 //   warps 9-10  MMA issuers, one per Q tile: S_t = Q_t K^T (SS, K-major) into
@@ -64,7 +66,10 @@ struct K1Cfg {
   static constexpr int kSlotBytes = kKTileBytes > kVTileBytes ? kKTileBytes : kVTileBytes;
   static constexpr int kSlots = DQK == 64 ? 8 : (DQK == 128 ? 4 : 2);
   static constexpr int kNumBars = 1 + 2 * kSlots + 6 * kQTiles + 1;
-  static constexpr int kBarOffset = kQTiles * kQTileBytes + kSlots * kSlotBytes;
+  // epilogue staging: one 32-row x 32-column fp32 box (4 KB, 128-byte swizzle) per softmax warp
+  static constexpr int kStageOffset = kQTiles * kQTileBytes + kSlots * kSlotBytes;
+  static constexpr int kStageBytes = 4 * kQTiles * 4096;
+  static constexpr int kBarOffset = kStageOffset + kStageBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 8 * kNumBars + 16;
   static constexpr uint32_t kColO = 256;
   static constexpr uint32_t kColP = kColO + kQTiles * DV;           // separate P columns, if they fit
@@ -204,7 +209,8 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, int w, Tile& T)
 template <int DQK, int DV>
 __global__ void __launch_bounds__(kK1Threads, 1)
     attn_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                        const __grid_constant__ AttnParams p) {
   using C = K1Cfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -444,6 +450,9 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         });
         // this issuer's S MMAs of the work tile are issued: Q may be reloaded once done
         mma_commit(bar_qempty);
+        // the tile's last PV goes out now, not behind the next tile's first S MMA (which
+        // waits for the next Q load): the epilogue waits for that PV
+        if (ok && C::kSepP) ok = flush();
       }
       if (ok) flush();
       // every MMA of this issuer (and the arrivals its commits make) completes before teardown
@@ -459,6 +468,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     const uint32_t tS = tmem + lane_base + t * kBlockN;
     const uint32_t tP = tmem + lane_base + C::col_p(t);
     const uint32_t tO = tmem + lane_base + C::kColO + t * DV;
+    uint8_t* const sStage = smem + C::kStageOffset + warp * 4096;  // this warp's epilogue box
     const float sl2 = p.scale_log2;
     int n = 0;  // steps (= PVs) of this Q tile over all work tiles
     bool ok = true;
@@ -590,6 +600,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       const int64_t orow = static_cast<int64_t>(T.itm.out_row0) + T.blk * kRowsPerCta + t * kBlockM + row;
       float* op = p.out + static_cast<int64_t>(T.itm.plane) * p.out_splane + orow * p.out_srow +
                   static_cast<int64_t>(T.h) * p.out_shead;
+      // A warp whose 32 rows are all valid writes O through shared memory and TMA stores
+      // (one 32 x 32 box per 32 columns): each thread's row lies a whole output row apart
+      // from its neighbour's, so direct stores would touch 32 cache lines per instruction.
+      const bool via_tma = p.out_tma && __all_sync(0xffffffffu, valid_row);
       if (nl > 0) {
         tc_fence_after_sync();
         // a row that saw no key keeps m = -inf; its l holds only the clamped 2^-125
@@ -606,7 +620,25 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_ofree[t]);
           }
-          if (valid_row) {
+          if (via_tma) {
+            // the buffer's previous box has been read by its store
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            // row `lane` of the box: 16-byte chunk i at chunk position i ^ (lane & 7) (128-byte swizzle)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                           __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+              *reinterpret_cast<float4*>(sStage + lane * 128 + ((i ^ (lane & 7)) * 16)) = v;
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              const int64_t z = static_cast<int64_t>(T.itm.plane) * p.out_plane_rows + orow;  // row of lane 0
+              tma_store_3d(&tm_o, sStage, 32 * c, T.h, static_cast<int>(z));
+              bulk_commit();
+            }
+          } else if (valid_row) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
@@ -624,6 +656,8 @@ __global__ void __launch_bounds__(kK1Threads, 1)
               static_cast<int64_t>(T.h) * p.lse_shead] = l > 0.f ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
       }
     }
+    // the O stores of this warp complete before the CTA releases its shared memory
+    if (lane == 0) bulk_wait_all();
   }
 
   __syncwarp();
@@ -646,8 +680,8 @@ int resident_ctas() {
 }
 
 template <int DQK, int DV>
-cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, AttnParams p,
-                        cudaStream_t stream) {
+cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                        AttnParams p, cudaStream_t stream) {
   using C = K1Cfg<DQK, DV>;
   if (p.n_items <= 0) return cudaSuccess;
   const WorkItem& last = p.items[p.n_items - 1];
@@ -659,7 +693,7 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_partial_kernel<DQK, DV><<<static_cast<unsigned>(grid), kK1Threads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  attn_partial_kernel<DQK, DV><<<static_cast<unsigned>(grid), kK1Threads, C::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -671,11 +705,11 @@ bool attn_partial_supported(int dqk, int dv) {
 }
 
 cudaError_t launch_attn_partial(int dqk, int dv, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const AttnParams& p, cudaStream_t stream) {
-  if (dqk == 64 && dv == 64) return launch_impl<64, 64>(tq, tk, tv, p, stream);
-  if (dqk == 128 && dv == 64) return launch_impl<128, 64>(tq, tk, tv, p, stream);
-  if (dqk == 128 && dv == 128) return launch_impl<128, 128>(tq, tk, tv, p, stream);
-  if (dqk == 192 && dv == 128) return launch_impl<192, 128>(tq, tk, tv, p, stream);
+                                const CUtensorMap& to, const AttnParams& p, cudaStream_t stream) {
+  if (dqk == 64 && dv == 64) return launch_impl<64, 64>(tq, tk, tv, to, p, stream);
+  if (dqk == 128 && dv == 64) return launch_impl<128, 64>(tq, tk, tv, to, p, stream);
+  if (dqk == 128 && dv == 128) return launch_impl<128, 128>(tq, tk, tv, to, p, stream);
+  if (dqk == 192 && dv == 128) return launch_impl<192, 128>(tq, tk, tv, to, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -47,6 +47,8 @@ struct AttnParams {
   float scale_log2;         // softmax scale * log2(e)
   float* out;               // fp32 partial output planes
   int64_t out_srow, out_shead, out_splane;
+  int32_t out_tma;          // 1: full 32-row warp chunks of out go through the O tensor map
+  int64_t out_plane_rows;   // rows per plane in the O tensor map's outer dimension
   float* lse;               // fp32 log-sum-exp planes
   int64_t lse_srow, lse_shead, lse_splane;
   int* status;              // device status word {code, site}
@@ -80,7 +82,8 @@ constexpr int kStatusTimeout = 1;
 
 // Host-side launchers (defined in attn_partial.cu / lse_merge.cu / status.cu).
 cudaError_t launch_attn_partial(int dqk, int dv, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, const AttnParams& p, cudaStream_t stream);
+                                const CUtensorMap& tv, const CUtensorMap& to, const AttnParams& p,
+                                cudaStream_t stream);
 bool attn_partial_supported(int dqk, int dv);
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_timeout_selftest(uint64_t limit_ns, int* status, cudaStream_t stream);
