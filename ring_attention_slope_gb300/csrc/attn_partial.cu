@@ -66,9 +66,12 @@ struct K1Cfg {
   static constexpr int kSlotBytes = kKTileBytes > kVTileBytes ? kKTileBytes : kVTileBytes;
   static constexpr int kSlots = DQK == 64 ? 8 : (DQK == 128 ? 4 : 2);
   static constexpr int kNumBars = 1 + 2 * kSlots + 6 * kQTiles + 1;
-  // epilogue staging: one 32-row x 32-column fp32 box (4 KB, 128-byte swizzle) per softmax warp
+  // epilogue staging: 32-row x 32-column fp32 boxes (4 KB each, 128-byte swizzle), two per
+  // softmax warp where shared memory allows (the second box is written while the first
+  // one's store still reads), else one
   static constexpr int kStageOffset = kQTiles * kQTileBytes + kSlots * kSlotBytes;
-  static constexpr int kStageBytes = 4 * kQTiles * 4096;
+  static constexpr int kStageBufs = kStageOffset + 2 * 4 * kQTiles * 4096 + 2048 <= 232448 ? 2 : 1;
+  static constexpr int kStageBytes = kStageBufs * 4 * kQTiles * 4096;
   static constexpr int kBarOffset = kStageOffset + kStageBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 8 * kNumBars + 16;
   static constexpr uint32_t kColO = 256;
@@ -190,8 +193,9 @@ struct Tile {
 // Work tile w -> (item, row block, head).  Consecutive w are the heads of one row
 // block (K/V shared in L2 by a KV group); items come heaviest first and an item's
 // later (heavier under the causal mask) row blocks before its earlier ones.
-__device__ __forceinline__ void decode_tile(const AttnParams& p, int w, Tile& T) {
-  int ii = 0;
+// `ii` carries the item index from the caller's previous work tile: a CTA visits its
+// tiles in increasing w, so the item index never decreases and the scan resumes there.
+__device__ __forceinline__ void decode_tile(const AttnParams& p, int w, Tile& T, int& ii) {
   while (ii < p.n_items - 1 && w >= (p.items[ii].cta_begin + p.items[ii].n_blocks) * p.Hq) ++ii;
   T.itm = p.items[ii];
   const int local = w - T.itm.cta_begin * p.Hq;
@@ -278,9 +282,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       uint32_t cnt = 0;
       int wt = 0;
       bool ok = true;
+      int item_hint = 0;
       for (int w = blockIdx.x; w < total; w += gridDim.x) {
         Tile T;
-        decode_tile(p, w, T);
+        decode_tile(p, w, T, item_hint);
         if (!has_steps(T.itm, p, T.geo)) continue;
         // Q of the previous work tile is in use until its last S MMAs are done
         if (wt > 0 && !wait_bounded(bar_qempty, (wt - 1) & 1, cta_abort, p.status, limit, 11)) {
@@ -393,9 +398,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
 
       bool ok = true;
       int wt = 0;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      int item_hint = 0;
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         Tile T;
-        decode_tile(p, w, T);
+        decode_tile(p, w, T, item_hint);
         if (!has_steps(T.itm, p, T.geo)) continue;
         if (!wait_bounded(bar_q, wt & 1, cta_abort, p.status, limit, 3)) {
           ok = false;
@@ -468,13 +474,14 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     const uint32_t tS = tmem + lane_base + t * kBlockN;
     const uint32_t tP = tmem + lane_base + C::col_p(t);
     const uint32_t tO = tmem + lane_base + C::kColO + t * DV;
-    uint8_t* const sStage = smem + C::kStageOffset + warp * 4096;  // this warp's epilogue box
+    uint8_t* const sStage = smem + C::kStageOffset + warp * (C::kStageBufs * 4096);  // this warp's boxes
     const float sl2 = p.scale_log2;
     int n = 0;  // steps (= PVs) of this Q tile over all work tiles
     bool ok = true;
+    int item_hint = 0;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       Tile T;
-      decode_tile(p, w, T);
+      decode_tile(p, w, T, item_hint);
       const int rows_t = t == 0 ? T.geo.rows[0] : T.geo.rows[1];
       if (rows_t <= 0) continue;
       const int q_pos = (t == 0 ? T.geo.qa[0] : T.geo.qa[1]) + row;
@@ -621,21 +628,28 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             if (lane == 0) mbar_arrive(&bar_ofree[t]);
           }
           if (via_tma) {
-            // the buffer's previous box has been read by its store
-            if (lane == 0) bulk_wait_read_all();
+            uint8_t* const box = sStage + (c % C::kStageBufs) * 4096;
+            // the store that last used this box has read it (with two boxes the most
+            // recent store, into the other box, may still be reading)
+            if (lane == 0) {
+              if (C::kStageBufs == 2)
+                bulk_wait_read_allbut1();
+              else
+                bulk_wait_read_all();
+            }
             __syncwarp();
             // row `lane` of the box: 16-byte chunk i at chunk position i ^ (lane & 7) (128-byte swizzle)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
                                            __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-              *reinterpret_cast<float4*>(sStage + lane * 128 + ((i ^ (lane & 7)) * 16)) = v;
+              *reinterpret_cast<float4*>(box + lane * 128 + ((i ^ (lane & 7)) * 16)) = v;
             }
             fence_proxy_async_shared();
             __syncwarp();
             if (lane == 0) {
               const int64_t z = static_cast<int64_t>(T.itm.plane) * p.out_plane_rows + orow;  // row of lane 0
-              tma_store_3d(&tm_o, sStage, 32 * c, T.h, static_cast<int>(z));
+              tma_store_3d(&tm_o, box, 32 * c, T.h, static_cast<int>(z));
               bulk_commit();
             }
           } else if (valid_row) {
