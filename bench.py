@@ -381,42 +381,49 @@ def merge_bytes_per_launch(slope, w, n, sizes, window):
 
 
 def run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier, dist):
+    """The metric through the host-buffer call: every step copies its inputs from pinned host memory and its
+    result back.  Two device-buffer sets alternate over three streams, so the copies of one step overlap the
+    compute of its neighbours (the library orders each buffer set's reuse); the timed region runs from the
+    first step's input copies to the last step's output copies."""
     hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
     hk = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
     hv = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
     hq.copy_(q)
     hk.copy_(k)
     hv.copy_(v)
-    ho = torch.empty((w.S, w.Hq, w.dv), dtype=torch.bfloat16, pin_memory=True)
-    hl = torch.empty((w.Hq, w.S), dtype=torch.float32, pin_memory=True)
-    dq, dk, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    out = torch.empty((w.S, w.Hq, w.dv), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((w.Hq, w.S), dtype=torch.float32, device="cuda")
+    sets = []
+    for _ in range(2):
+        sets.append({"q": torch.empty_like(q), "k": torch.empty_like(k), "v": torch.empty_like(v),
+                     "out": torch.empty((w.S, w.Hq, w.dv), dtype=torch.bfloat16, device="cuda"),
+                     "lse": torch.empty((w.Hq, w.S), dtype=torch.float32, device="cuda"),
+                     "hout": torch.empty((w.S, w.Hq, w.dv), dtype=torch.bfloat16, pin_memory=True),
+                     "hlse": torch.empty((w.Hq, w.S), dtype=torch.float32, pin_memory=True)})
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv_.copy_(hv, non_blocking=True)
-        slope.cp_prefill(dq, dk, dv_, n, w.layout, chunk_sizes=sizes, window=window, out=out, lse=lse,
-                         workspace=ws)
-        ho.copy_(out, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+    def step(i):
+        b = sets[i % 2]
+        slope.cp_prefill_host(hq, hk, hv, b["hout"], b["hlse"], b["q"], b["k"], b["v"], b["out"], b["lse"], n,
+                              w.layout, chunk_sizes=sizes, window=window, workspace=ws, copy_in_stream=s_in,
+                              compute_stream=stream, copy_out_stream=s_out)
 
-    for _ in range(max(1, args.warmup)):
-        step()
+    for i in range(max(1, args.warmup)):
+        step(i)
     torch.cuda.synchronize()
     barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        step()
-    b.record(stream)
+    a.record(s_in)
+    for i in range(args.steps):
+        step(i)
+    b.record(s_out)
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b), dist, "cuda")
     world = dist.get_world_size() if dist is not None else 1
     val = job_tflops(workload_flops(w, window), args.steps, world, ms)
-    return {"value": val, "unit": UNIT, "h2d_bytes_per_step": int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2),
-            "d2h_bytes_per_step": int(ho.numel() * 2 + hl.numel() * 4), "ms_per_step": ms / args.steps}
+    h2d = int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2)
+    d2h = int(sets[0]["hout"].numel() * 2 + sets[0]["hlse"].numel() * 4)
+    return {"value": val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms / args.steps, "api": "slope_cp_prefill_host",
+            "overlap": "2 device-buffer sets; input copies, compute and output copies on 3 streams"}
 
 
 def main():

@@ -186,6 +186,44 @@ SLOPE_API size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t 
                                        const int64_t* chunk_sizes);
 
 /*
+ * slope_cp_prefill on inputs and outputs in host memory: the same attention
+ * (Moreh, "Optimizing long-context prefill on multiple older-generation GPU
+ * nodes", section "Introduction to Context Parallelism"), with the copies
+ * to and from the GPU queued by the library, on three caller streams:
+ *   copy_in_stream   host q/k/v -> the device buffers q/k/v,
+ *   compute_stream   slope_cp_prefill on the device buffers (after the copies),
+ *   copy_out_stream  device out/lse -> host out/lse (after the compute).
+ *
+ *   q_host, k_host, v_host, out_host, lse_host: host tensors (pinned memory
+ *     for asynchronous copies), each dense (row-major, no padding) and of the
+ *     same shape and dtype as its device buffer.  lse_host and lse are both
+ *     NULL or both given.
+ *   q, k, v, out, lse: caller-owned device buffers, dense; the other
+ *     arguments are those of slope_cp_prefill.
+ *
+ * Nothing is allocated.  The call returns once the work is queued; the host
+ * outputs are valid when copy_out_stream reaches that point.  Two calls with
+ * different device buffers overlap: the second call's input copies run while
+ * the first computes, and the first call's output copies while the second
+ * computes (the workspace is shared safely: both computes run on
+ * compute_stream).  A call that reuses the device buffers of an earlier call
+ * (same device, same q buffer) is ordered after it by events: its input
+ * copies wait until the earlier compute has read the inputs, and its compute
+ * waits until the earlier output copies have read out/lse.  The library
+ * tracks 16 such buffer sets per process; taking a slot from a 17th set first
+ * waits on the host for the oldest set's last call.  Argument errors return
+ * a status before anything is queued.
+ */
+SLOPE_API slope_status slope_cp_prefill_host(const slope_tensor* q_host, const slope_tensor* k_host,
+                                             const slope_tensor* v_host, slope_tensor* out_host,
+                                             slope_tensor* lse_host, const slope_tensor* q, const slope_tensor* k,
+                                             const slope_tensor* v, slope_tensor* out, slope_tensor* lse,
+                                             int n_chunks, slope_layout layout, const int64_t* chunk_sizes,
+                                             int causal, int64_t window, float scale, void* workspace,
+                                             size_t workspace_bytes, void* copy_in_stream, void* compute_stream,
+                                             void* copy_out_stream);
+
+/*
  * Same as slope_cp_prefill, and additionally records a pair of CUDA events
  * around every kernel launch it makes, on `stream`: events[2*i] before launch
  * i and events[2*i+1] after it.  events is a host array of 2*n_event_pairs

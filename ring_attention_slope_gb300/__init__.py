@@ -56,7 +56,7 @@ _lib = None
 EXPORTED = ["slope_attn_partial", "slope_lse_merge", "slope_cp_prefill", "slope_cp_prefill_workspace_size",
             "slope_cp_prefill_timed", "slope_cp_prefill_plan", "slope_device_status",
             "slope_debug_timeout_selftest", "slope_status_string", "slope_version", "slope_last_error",
-            "slope_cp_prefill_static_scratch"]
+            "slope_cp_prefill_static_scratch", "slope_cp_prefill_host"]
 
 
 def build(force: bool = False) -> str:
@@ -102,6 +102,9 @@ def load():
     lib.slope_last_error.restype = ctypes.c_char_p
     lib.slope_cp_prefill_static_scratch.argtypes = [T, T, T, c_int, c_int, P(i64), c_int, i64, f32, T, T, vp]
     lib.slope_cp_prefill_static_scratch.restype = c_int
+    lib.slope_cp_prefill_host.argtypes = [T, T, T, T, T, T, T, T, T, T, c_int, c_int, P(i64), c_int, i64, f32, vp,
+                                          ctypes.c_size_t, vp, vp, vp]
+    lib.slope_cp_prefill_host.restype = c_int
     _lib = lib
     return lib
 
@@ -121,8 +124,8 @@ def _torch():
     return torch
 
 
-def _desc(t, expect_dtype=None):
-    """slope_tensor describing a CUDA tensor (view) of rank 2 or 3."""
+def _desc(t, expect_dtype=None, host=False):
+    """slope_tensor describing a CUDA tensor (or, with host=True, a CPU tensor) of rank 2 or 3."""
     torch = _torch()
     if t.dtype == torch.bfloat16:
         dt = _BF16
@@ -132,8 +135,8 @@ def _desc(t, expect_dtype=None):
         raise TypeError(f"unsupported dtype {t.dtype}")
     if expect_dtype is not None and t.dtype != expect_dtype:
         raise TypeError(f"expected {expect_dtype}, got {t.dtype}")
-    if t.numel() > 0 and t.device.type != "cuda":
-        raise TypeError("libslope operates on CUDA tensors")
+    if t.numel() > 0 and t.device.type != ("cpu" if host else "cuda"):
+        raise TypeError("expected a host (CPU) tensor" if host else "libslope operates on CUDA tensors")
     if t.dim() not in (2, 3):
         raise ValueError("tensors must be rank 2 or 3")
     d = SlopeTensor()
@@ -250,6 +253,36 @@ def cp_prefill(q, k, v, n_chunks, layout="zigzag", *, chunk_sizes=None, causal=T
                                  ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
     _check(st, "slope_cp_prefill")
     return out, lse
+
+
+def cp_prefill_host(q_host, k_host, v_host, out_host, lse_host, q, k, v, out, lse, n_chunks, layout="zigzag", *,
+                    chunk_sizes=None, causal=True, window=0, scale=0.0, workspace=None, copy_in_stream=None,
+                    compute_stream=None, copy_out_stream=None):
+    """cp_prefill on host tensors: queues host->device copies of q/k/v into the device buffers q/k/v on
+    ``copy_in_stream``, the prefill on ``compute_stream`` and device->host copies of out/lse into
+    out_host/lse_host on ``copy_out_stream`` (streams default to the current stream).  All tensors are dense;
+    host tensors should be pinned.  Returns immediately; the host outputs are valid once
+    ``copy_out_stream`` has reached this point.  Calls on different device buffers overlap (see
+    slope_cp_prefill_host in include/slope.h)."""
+    if workspace is None:
+        S, Hq, _ = q.shape
+        nbytes = cp_prefill_workspace_size(S, Hq, v.shape[2], n_chunks, layout, chunk_sizes)
+        if nbytes == 0:
+            raise SlopeError(-5, "slope_cp_prefill_workspace_size")
+        workspace = _torch().empty((nbytes,), dtype=_torch().uint8, device=q.device)
+    arr, ptr = _chunk_array(chunk_sizes)
+    hq, hk, hv, ho = (_desc(t, host=True) for t in (q_host, k_host, v_host, out_host))
+    hl = _desc(lse_host, host=True) if lse_host is not None else None
+    dq, dk, dvv, do = _desc(q), _desc(k), _desc(v), _desc(out)
+    dl = _desc(lse) if lse is not None else None
+    ref = lambda d: ctypes.byref(d) if d is not None else None  # noqa: E731
+    st = load().slope_cp_prefill_host(ref(hq), ref(hk), ref(hv), ref(ho), ref(hl), ref(dq), ref(dk), ref(dvv),
+                                      ref(do), ref(dl), int(n_chunks), _layout(layout), ptr, int(bool(causal)),
+                                      int(window), float(scale), ctypes.c_void_p(workspace.data_ptr()),
+                                      workspace.numel(), _stream_ptr(copy_in_stream), _stream_ptr(compute_stream),
+                                      _stream_ptr(copy_out_stream))
+    _check(st, "slope_cp_prefill_host")
+    return workspace
 
 
 def cp_prefill_static_scratch(q, k, v, n_chunks, layout="zigzag", *, chunk_sizes=None, causal=True, window=0,

@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "kernels.cuh"
@@ -347,10 +348,11 @@ WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t dv, int n_planes
   return w;
 }
 
-slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
-                             slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
-                             float scale, slope_tensor* out, slope_tensor* lse, void* workspace,
-                             size_t workspace_bytes, cudaStream_t stream, Timing* tm) {
+// Every argument check of cp_prefill_impl, with no side effect; fills `plan`.
+slope_status cp_prefill_check(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
+                              slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
+                              const slope_tensor* out, const slope_tensor* lse, const void* workspace,
+                              size_t workspace_bytes, Plan& plan) {
   slope_status st;
   if ((st = check_qkv(q)) != SLOPE_OK || (st = check_qkv(k)) != SLOPE_OK || (st = check_qkv(v)) != SLOPE_OK)
     return st;
@@ -363,11 +365,25 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   if ((st = check_out(out, S, Hq, dv, true)) != SLOPE_OK) return st;
   if (lse != nullptr && (st = check_lse(lse, Hq, S)) != SLOPE_OK) return st;
   if (S == 0) return SLOPE_ERR_SHAPE;
-  Plan plan;
   if ((st = build_plan(S, n_chunks, layout, chunk_sizes, causal, window, plan)) != SLOPE_OK) return st;
   if (plan.n_planes > kMaxMerge) return SLOPE_ERR_UNSUPPORTED;
   const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < wl.total) return SLOPE_ERR_WORKSPACE;
+  return SLOPE_OK;
+}
+
+slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
+                             slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
+                             float scale, slope_tensor* out, slope_tensor* lse, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream, Timing* tm) {
+  slope_status st;
+  Plan plan;
+  if ((st = cp_prefill_check(q, k, v, n_chunks, layout, chunk_sizes, causal, window, out, lse, workspace,
+                             workspace_bytes, plan)) != SLOPE_OK)
+    return st;
+  const int64_t S = q->shape[0], Hq = q->shape[1], dqk = q->shape[2];
+  const int64_t Hkv = k->shape[1], dv = v->shape[2];
+  const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes);
   int* status = device_status_ptr();
   if (status == nullptr) return cuda_fail("device status word (cudaGetSymbolAddress)");
 
@@ -487,6 +503,81 @@ void* static_scratch_ptr() {
 }  // namespace
 
 // ==================================================================== exported
+
+// ---------------------------------------------------------------- host-buffer prefill
+
+namespace {
+
+// A dense (row-major, no padding) tensor: the host copy and its device buffer are then
+// one contiguous block each, moved by one cudaMemcpyAsync.
+bool dense(const slope_tensor* t) {
+  if (t->ndim == 3) return t->stride[2] == 1 && t->stride[1] == t->shape[2] && t->stride[0] == t->shape[1] * t->shape[2];
+  if (t->ndim == 2) return t->stride[1] == 1 && t->stride[0] == t->shape[1];
+  return false;
+}
+bool same_shape(const slope_tensor* a, const slope_tensor* b) {
+  if (a->ndim != b->ndim || a->dtype != b->dtype) return false;
+  for (int i = 0; i < a->ndim; ++i)
+    if (a->shape[i] != b->shape[i]) return false;
+  return true;
+}
+size_t tensor_bytes(const slope_tensor* t) {
+  size_t n = t->dtype == SLOPE_BF16 ? 2 : 4;
+  for (int i = 0; i < t->ndim; ++i) n *= static_cast<size_t>(t->shape[i]);
+  return n;
+}
+
+// Ordering between calls that reuse one set of device buffers, keyed by (device, q buffer):
+// `in_ready`  the input copies into the buffers are done,
+// `consumed`  the compute that read them (and wrote out/lse) is done,
+// `drained`   the output copies that read out/lse are done.
+struct BufferSetEvents {
+  int device = -1;
+  const void* key = nullptr;
+  cudaEvent_t in_ready = nullptr, consumed = nullptr, drained = nullptr;
+  bool used = false;  // events hold the records of an earlier call
+};
+constexpr int kBufferSets = 16;
+std::mutex g_buffer_sets_mutex;
+BufferSetEvents g_buffer_sets[kBufferSets];
+int g_buffer_sets_next = 0;
+
+// The entry of (device, key), creating it (or taking the oldest slot) if absent.  A slot
+// taken from another buffer set first waits (on the host) for that set's last call to
+// finish, so a later call on the evicted set starts with no work of its own pending.
+BufferSetEvents* buffer_set(int device, const void* key) {
+  for (auto& b : g_buffer_sets)
+    if (b.device == device && b.key == key) return &b;
+  BufferSetEvents& b = g_buffer_sets[g_buffer_sets_next];
+  g_buffer_sets_next = (g_buffer_sets_next + 1) % kBufferSets;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return nullptr;
+  if (b.in_ready != nullptr) {
+    if (b.device != cur && cudaSetDevice(b.device) != cudaSuccess) return nullptr;
+    if (b.used) cudaEventSynchronize(b.drained);
+    if (b.device != device) {
+      cudaEventDestroy(b.in_ready);
+      cudaEventDestroy(b.consumed);
+      cudaEventDestroy(b.drained);
+      b.in_ready = b.consumed = b.drained = nullptr;
+    }
+    if (b.device != cur && cudaSetDevice(cur) != cudaSuccess) return nullptr;
+  }
+  b.used = false;
+  b.key = key;
+  b.device = device;
+  if (b.in_ready == nullptr &&
+      (cudaEventCreateWithFlags(&b.in_ready, cudaEventDisableTiming) != cudaSuccess ||
+       cudaEventCreateWithFlags(&b.consumed, cudaEventDisableTiming) != cudaSuccess ||
+       cudaEventCreateWithFlags(&b.drained, cudaEventDisableTiming) != cudaSuccess)) {
+    b.device = -1;
+    b.key = nullptr;
+    return nullptr;
+  }
+  return &b;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -666,6 +757,68 @@ slope_status slope_cp_prefill_timed(const slope_tensor* q, const slope_tensor* k
                                     workspace, workspace_bytes, static_cast<cudaStream_t>(stream), &tm);
   *n_launches = tm.count;
   return st;
+}
+
+slope_status slope_cp_prefill_host(const slope_tensor* q_host, const slope_tensor* k_host,
+                                   const slope_tensor* v_host, slope_tensor* out_host, slope_tensor* lse_host,
+                                   const slope_tensor* q, const slope_tensor* k, const slope_tensor* v,
+                                   slope_tensor* out, slope_tensor* lse, int n_chunks, slope_layout layout,
+                                   const int64_t* chunk_sizes, int causal, int64_t window, float scale,
+                                   void* workspace, size_t workspace_bytes, void* copy_in_stream,
+                                   void* compute_stream, void* copy_out_stream) {
+  if (q_host == nullptr || k_host == nullptr || v_host == nullptr || out_host == nullptr || q == nullptr ||
+      k == nullptr || v == nullptr || out == nullptr)
+    return SLOPE_ERR_NULL;
+  if ((lse_host == nullptr) != (lse == nullptr)) return SLOPE_ERR_NULL;
+  const slope_tensor* pairs[5][2] = {{q_host, q}, {k_host, k}, {v_host, v}, {out_host, out}, {lse_host, lse}};
+  for (auto& pr : pairs) {
+    if (pr[0] == nullptr) continue;
+    if (!same_shape(pr[0], pr[1])) return SLOPE_ERR_SHAPE;
+    if (!dense(pr[0]) || !dense(pr[1])) return SLOPE_ERR_STRIDE;
+    if (tensor_bytes(pr[0]) > 0 && pr[0]->data == nullptr) return SLOPE_ERR_NULL;
+  }
+  // every check of the compute runs before anything is queued
+  Plan probe;
+  slope_status st = cp_prefill_check(q, k, v, n_chunks, layout, chunk_sizes, causal, window, out, lse, workspace,
+                                     workspace_bytes, probe);
+  if (st != SLOPE_OK) return st;
+  if (out->dtype != SLOPE_BF16 && out->dtype != SLOPE_F32) return SLOPE_ERR_DTYPE;
+  int device = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&device)) != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  auto s_in = static_cast<cudaStream_t>(copy_in_stream);
+  auto s_c = static_cast<cudaStream_t>(compute_stream);
+  auto s_out = static_cast<cudaStream_t>(copy_out_stream);
+  std::lock_guard<std::mutex> guard(g_buffer_sets_mutex);
+  BufferSetEvents* b = buffer_set(device, q->data);
+  if (b == nullptr) return cuda_fail("cudaEventCreateWithFlags (buffer-set events)");
+  // inputs: after the previous compute on these buffers has read them
+  if (b->used && (e = cudaStreamWaitEvent(s_in, b->consumed, 0)) != cudaSuccess)
+    return cuda_fail("cudaStreamWaitEvent", e);
+  for (int i = 0; i < 3; ++i)
+    if ((e = cudaMemcpyAsync(const_cast<void*>(pairs[i][1]->data), pairs[i][0]->data, tensor_bytes(pairs[i][0]),
+                             cudaMemcpyHostToDevice, s_in)) != cudaSuccess)
+      return cuda_fail("cudaMemcpyAsync (host to device)", e);
+  if ((e = cudaEventRecord(b->in_ready, s_in)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
+  // compute: after the inputs, and after the previous output copies have read out/lse
+  if ((e = cudaStreamWaitEvent(s_c, b->in_ready, 0)) != cudaSuccess) return cuda_fail("cudaStreamWaitEvent", e);
+  if (b->used && (e = cudaStreamWaitEvent(s_c, b->drained, 0)) != cudaSuccess)
+    return cuda_fail("cudaStreamWaitEvent", e);
+  st = cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, out, lse, workspace,
+                       workspace_bytes, s_c, nullptr);
+  if (st != SLOPE_OK) return st;
+  if ((e = cudaEventRecord(b->consumed, s_c)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
+  // outputs: after the compute
+  if ((e = cudaStreamWaitEvent(s_out, b->consumed, 0)) != cudaSuccess) return cuda_fail("cudaStreamWaitEvent", e);
+  for (int i = 3; i < 5; ++i) {
+    if (pairs[i][0] == nullptr) continue;
+    if ((e = cudaMemcpyAsync(pairs[i][0]->data, pairs[i][1]->data, tensor_bytes(pairs[i][1]),
+                             cudaMemcpyDeviceToHost, s_out)) != cudaSuccess)
+      return cuda_fail("cudaMemcpyAsync (device to host)", e);
+  }
+  if ((e = cudaEventRecord(b->drained, s_out)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
+  b->used = true;
+  return SLOPE_OK;
 }
 
 int64_t slope_cp_prefill_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,

@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_symbols()
-    assert len(names) == 12, names
+    assert len(names) == 13, names
     for n in names:
         assert hasattr(lib, n), f"{n} declared in slope.h but not exported"
     assert sorted(names) == sorted(slope.EXPORTED)
@@ -117,3 +117,28 @@ def test_workspace_size(lib):
     assert wc >= 2 * 65536 * 64 * 65 * 4
     assert slope.cp_prefill_workspace_size(1000, 4, 64, 8, "zigzag") == 0
     assert slope.cp_prefill_workspace_size(1024, 4, 96, 4, "zigzag") == 0
+
+
+def test_cp_prefill_host_argument_errors(lib):
+    """Every argument error of the host-buffer prefill returns before anything is queued (no GPU here)."""
+    S, Hq, Hkv, d = 1024, 4, 1, 64
+    q, k, v = _t([S, Hq, d]), _t([S, Hkv, d]), _t([S, Hkv, d])
+    out, lse = _t([S, Hq, d]), _t([Hq, S], dtype=1)
+    hq, hk, hv = _t([S, Hq, d], data=0x90000), _t([S, Hkv, d], data=0x90000), _t([S, Hkv, d], data=0x90000)
+    hout, hlse = _t([S, Hq, d], data=0x90000), _t([Hq, S], dtype=1, data=0x90000)
+
+    def call(hq=hq, hk=hk, hv=hv, hout=hout, hlse=hlse, q=q, k=k, v=v, out=out, lse=lse, ws=0x20000,
+             ws_bytes=1 << 40, n=4):
+        r = lambda t: ctypes.byref(t) if t is not None else None  # noqa: E731
+        return lib.slope_cp_prefill_host(r(hq), r(hk), r(hv), r(hout), r(hlse), r(q), r(k), r(v), r(out), r(lse),
+                                         n, 1, None, 1, 0, 0.0, ws, ws_bytes, None, None, None)
+
+    assert call(hq=None) == E_NULL
+    assert call(hlse=None) == E_NULL                                   # lse given, lse_host not
+    assert call(hk=_t([S, Hkv + 1, d], data=0x90000)) == E_SHAPE       # host/device shapes differ
+    assert call(hout=_t([S, Hq, d], dtype=1, data=0x90000)) == E_SHAPE  # host/device dtypes differ
+    assert call(hv=_t([S, Hkv, d], data=0x90000, stride=[2 * Hkv * d, d, 1])) == E_STRIDE  # not dense
+    assert call(q=_t([S, Hq, d], stride=[Hq * d + 8, d, 1]), hq=_t([S, Hq, d], data=0x90000,
+                                                                    stride=[Hq * d + 8, d, 1])) == E_STRIDE
+    assert call(ws=0) == E_WS                                          # the compute's own checks run first
+    assert call(n=5) == E_LAYOUT

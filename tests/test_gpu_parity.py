@@ -295,3 +295,34 @@ def test_full_s100k_zigzag16(window):
 
 def test_full_mla_s64k_chunked_var():
     check_full_workload(wl.WORKLOADS[4], 0)
+
+
+@pytest.mark.parametrize("layout,n", [("zigzag", 4), ("chunked", 3)])
+def test_cp_prefill_host_buffers_overlapped_calls(layout, n):
+    """Three host-buffer prefills on two alternating device-buffer sets and three streams: each host
+    result equals slope_cp_prefill on the same inputs, bit for bit (the third call reuses the first
+    call's device buffers while the second call's work may still run)."""
+    S, Hq, Hkv, d = 2048, 8, 2, 64
+    calls = [qkv(S, Hq, Hkv, d, d, seed=90 + i, device="cpu") for i in range(3)]
+    hosts = [tuple(t.pin_memory() for t in c) for c in calls]
+    sets = [dict(q=torch.empty(S, Hq, d, dtype=torch.bfloat16, device="cuda"),
+                 k=torch.empty(S, Hkv, d, dtype=torch.bfloat16, device="cuda"),
+                 v=torch.empty(S, Hkv, d, dtype=torch.bfloat16, device="cuda"),
+                 out=torch.empty(S, Hq, d, dtype=torch.bfloat16, device="cuda"),
+                 lse=torch.empty(Hq, S, dtype=torch.float32, device="cuda")) for _ in range(2)]
+    houts = [torch.empty(S, Hq, d, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    hlses = [torch.empty(Hq, S, dtype=torch.float32).pin_memory() for _ in range(3)]
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ws = None
+    for i in range(3):
+        b = sets[i % 2]
+        ws = slope.cp_prefill_host(*hosts[i], houts[i], hlses[i], b["q"], b["k"], b["v"], b["out"], b["lse"], n,
+                                   layout, workspace=ws, copy_in_stream=s_in, compute_stream=s_c,
+                                   copy_out_stream=s_out)
+    torch.cuda.synchronize()
+    for i in range(3):
+        ro, rl = slope.cp_prefill(*(t.cuda() for t in calls[i]), n, layout)
+        torch.cuda.synchronize()
+        assert torch.equal(houts[i], ro.cpu()), f"call {i}: out differs"
+        assert torch.equal(hlses[i], rl.cpu()), f"call {i}: lse differs"
+    assert slope.device_status() == (0, 0)
