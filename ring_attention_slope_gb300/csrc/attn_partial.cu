@@ -493,16 +493,21 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       auto step = [&](const bool full, const int kpos, const int valid) -> bool {
         if (!warp_all(wait_bounded(&bar_s[t], n & 1, cta_abort, p.status, limit, 8))) return false;
         tc_fence_after_sync();
+        // S_t with the maximum of each 32-column quarter of the row (taken by the load)
         uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(tS + 0, r0);
-        tmem_ld32(tS + 32, r1);
-        tmem_ld32(tS + 64, r2);
-        tmem_ld32(tS + 96, r3);
+        float q0 = tmem_ld32_max(tS + 0, r0);
+        float q1 = tmem_ld32_max(tS + 32, r1);
+        float q2 = tmem_ld32_max(tS + 64, r2);
+        float q3 = tmem_ld32_max(tS + 96, r3);
         tmem_ld_wait();
         reg_fence(r0);
         reg_fence(r1);
         reg_fence(r2);
         reg_fence(r3);
+        reg_fence(q0);
+        reg_fence(q1);
+        reg_fence(q2);
+        reg_fence(q3);
         if (C::kSepP) {  // S_t is in registers: the next S MMA of this tile may overwrite it
           tc_fence_before_sync();
           __syncwarp();
@@ -516,6 +521,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           sv[64 + i] = __uint_as_float(r2[i]);
           sv[96 + i] = __uint_as_float(r3[i]);
         }
+        float mx = fmax3(q0, q1, fmaxf(q2, q3));  // row max of a fully visible tile
         if (!full) {
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c) {
@@ -523,19 +529,19 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             const bool vis = c < valid && (!p.causal || kp <= q_pos) && (p.window == 0 || q_pos - kp < p.window);
             if (!vis) sv[c] = -INFINITY;
           }
-        }
-        // row max: four independent chains of 3-input max
-        float a0 = sv[0], a1 = sv[1], a2 = sv[2], a3 = sv[3];
+          // row max over the visible scores: four independent chains of 3-input max
+          float a0 = sv[0], a1 = sv[1], a2 = sv[2], a3 = sv[3];
 #pragma unroll
-        for (int i = 4; i < 124; i += 8) {
-          a0 = fmax3(a0, sv[i], sv[i + 1]);
-          a1 = fmax3(a1, sv[i + 2], sv[i + 3]);
-          a2 = fmax3(a2, sv[i + 4], sv[i + 5]);
-          a3 = fmax3(a3, sv[i + 6], sv[i + 7]);
+          for (int i = 4; i < 124; i += 8) {
+            a0 = fmax3(a0, sv[i], sv[i + 1]);
+            a1 = fmax3(a1, sv[i + 2], sv[i + 3]);
+            a2 = fmax3(a2, sv[i + 4], sv[i + 5]);
+            a3 = fmax3(a3, sv[i + 6], sv[i + 7]);
+          }
+          a0 = fmax3(a0, sv[124], sv[125]);
+          a1 = fmax3(a1, sv[126], sv[127]);
+          mx = fmax3(a0, a1, fmaxf(a2, a3));
         }
-        a0 = fmax3(a0, sv[124], sv[125]);
-        a1 = fmax3(a1, sv[126], sv[127]);
-        const float mx = fmax3(a0, a1, fmaxf(a2, a3));
         const float m_new = mx * sl2;
         const bool need = m_new > m_used + kRescaleThreshold;
         const bool any_need = __any_sync(0xffffffffu, need);
