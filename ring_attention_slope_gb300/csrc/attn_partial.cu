@@ -45,15 +45,17 @@ constexpr int kMmaWarp = kTmaWarp + 1;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 // Of every 16 element pairs of a score row, this many take 2^x on the FMA pipe
-// (softmax_pair_poly) and the rest on the MUFU unit, which bounds the softmax: with two
-// softmax warps per SM sub-partition, 2 ex2 cost 8 MUFU cycles and the polynomial pair
-// about 14 more FMA-pipe cycles and 8 more issue slots than the MUFU pair.  Measured on
-// the causal 32K zigzag workload (kernel TFLOP/s): 0 -> 745, 1 -> 749, 2 -> 765,
-// 3 -> 696, 4 -> 685 (beyond 2 the register spills and the issue slots win).  A masked
-// score (-inf) gives 2^-125 there instead of 0: once a row has seen a key its sum l is
-// >= 1 and the term is far below bf16 resolution; before that the row's max is -inf
-// and the first visible key rescales l and O by 0; a row that never sees a key writes 0.
-constexpr int kPolyPairsPer16 = 2;
+// (softmax_pair_poly) instead of the MUFU unit.  With two softmax warps per SM
+// sub-partition, 2 ex2 cost 8 MUFU cycles and the polynomial pair about 14 more FMA-pipe
+// cycles and 8 more issue slots than the MUFU pair.  That paid while the row max was a
+// tree of 3-input max instructions (kernel TFLOP/s on the causal 32K zigzag workload:
+// 0 -> 745, 1 -> 749, 2 -> 765, 3 -> 696); since the TMEM load takes the row max, the
+// MUFU-only loop is fastest (0 -> 954, 1 -> 927, 2 -> 917, 3 -> 885), so the
+// polynomial is compiled out.  With pairs on the polynomial, a masked score (-inf)
+// gives 2^-125 instead of 0: once a row has seen a key its sum l is >= 1 and the term
+// is far below bf16 resolution; before that the row's max is -inf and the first
+// visible key rescales l and O by 0; a row that never sees a key writes 0.
+constexpr int kPolyPairsPer16 = 0;
 
 template <int DQK, int DV>
 struct K1Cfg {
