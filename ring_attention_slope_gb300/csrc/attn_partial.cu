@@ -67,7 +67,7 @@ struct K1Cfg {
   static constexpr int kVTileBytes = kVChunks * kChunkBytes;
   static constexpr int kSlotBytes = kKTileBytes > kVTileBytes ? kKTileBytes : kVTileBytes;
   static constexpr int kSlots = DQK == 64 ? 8 : (DQK == 128 ? 4 : 2);
-  static constexpr int kNumBars = 1 + 2 * kSlots + 6 * kQTiles + 1;
+  static constexpr int kNumBars = 1 + 2 * kSlots + 6 * kQTiles + 1 + 4 * kQTiles;
   // epilogue staging: 32-row x 32-column fp32 boxes (4 KB each, 128-byte swizzle), two per
   // softmax warp where shared memory allows (the second box is written while the first
   // one's store still reads), else one
@@ -83,6 +83,10 @@ struct K1Cfg {
   static_assert(kColO + kQTiles * DV <= 512, "TMEM budget");
   // TMEM column of P_t
   __device__ static constexpr uint32_t col_p(int t) { return kSepP ? kColP + t * (kBlockN / 2) : t * kBlockN; }
+  // The two softmax warps of an SM sub-partition take turns on their exponentials where P
+  // overwrites S (dv = 128).  Measured (kernel TFLOP/s): MLA shape 192/128 1141 -> 1220
+  // with turns; at dv = 64 turns cost more than they save (causal 32K zigzag 956 -> 920).
+  static constexpr bool kTurns = !kSepP;
 };
 
 __device__ __forceinline__ int floor_div(int a, int b) {
@@ -233,7 +237,8 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   uint64_t* bar_qempty = bar_ofree + kQTiles;
   uint64_t* bar_drain = bar_qempty + 1;  // one per MMA issuer
   uint64_t* bar_sfree = bar_drain + kQTiles;  // softmax t has loaded S_t into registers
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_sfree + kQTiles);
+  uint64_t* bar_turn = bar_sfree + kQTiles;    // [t * 4 + wq]: softmax warp (t, wq) may exponentiate
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_turn + 4 * kQTiles);
   volatile int* cta_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -264,6 +269,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(&bar_drain[t], 1);
       mbar_init(&bar_sfree[t], 4);  // one arrival per softmax warp
+      for (int q = 0; q < 4; ++q) mbar_init(&bar_turn[t * 4 + q], 1);  // lane 0 of the partner warp
     }
     fence_barrier_init();
   }
@@ -477,6 +483,24 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     const uint32_t tP = tmem + lane_base + C::col_p(t);
     const uint32_t tO = tmem + lane_base + C::kColO + t * DV;
     uint8_t* const sStage = smem + C::kStageOffset + warp * (C::kStageBufs * 4096);  // this warp's boxes
+    // Where C::kTurns holds, the softmax warps of the two Q tiles that share an SM
+    // sub-partition (same wq) take turns on their exponentials, which the sub-partition's
+    // MUFU unit bounds: one warp
+    // exponentiates alone while the other loads S, stores P and waits for the MMAs.
+    // Turn k of tile 0 waits for tile 1's turn k-1, turn k of tile 1 for tile 0's turn k.
+    // Both take one turn per step of whichever tile has more steps in the work tile; the
+    // tile with fewer steps passes its extra turns without work, so the turns stay paired.
+    int turn = 0;
+    auto take_turn = [&]() -> bool {
+      if (t == 0 && turn == 0) return true;
+      const uint32_t par = static_cast<uint32_t>(t == 0 ? turn - 1 : turn) & 1u;
+      return warp_all(wait_bounded(&bar_turn[t * 4 + wq], par, cta_abort, p.status, limit, 13));
+    };
+    auto pass_turn = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_turn[(t ^ 1) * 4 + wq]);
+      ++turn;
+    };
     const float sl2 = p.scale_log2;
     int n = 0;  // steps (= PVs) of this Q tile over all work tiles
     bool ok = true;
@@ -485,7 +509,31 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       Tile T;
       decode_tile(p, w, T, item_hint);
       const int rows_t = t == 0 ? T.geo.rows[0] : T.geo.rows[1];
-      if (rows_t <= 0) continue;
+      // turns of this work tile: the step count of the tile with more steps
+      int n_turns = 0;
+      if (C::kTurns) {
+        int cnt[kQTiles] = {0, 0};
+#pragma unroll
+        for (int u = 0; u < kQTiles; ++u) {
+          if (T.geo.rows[u] <= 0) continue;
+          for (int r = 0; r < T.itm.n_kv; ++r) {
+            const TileRange R = tile_range(r == 0 ? T.itm.kv[0].row0 : T.itm.kv[1].row0,
+                                           r == 0 ? T.itm.kv[0].len : T.itm.kv[1].len, T.geo.qa[u], T.geo.qb[u], p);
+            cnt[u] += max(0, R.hi - R.lo + 1);
+          }
+        }
+        n_turns = max(cnt[0], cnt[1]);
+      }
+      int taken = 0;  // turns taken in this work tile
+      if (rows_t <= 0) {
+        if constexpr (C::kTurns) {
+          for (; taken < n_turns && ok; ++taken) {
+            ok = take_turn();
+            if (ok) pass_turn();
+          }
+        }
+        continue;
+      }
       const int q_pos = (t == 0 ? T.geo.qa[0] : T.geo.qa[1]) + row;
       float m_used = -INFINITY;  // running max in log2-scaled units
       float l = 0.f;             // running sum of exp2(s*sl2 - m_used)
@@ -555,6 +603,9 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
         // p = exp2(s * sl2 - m), packed to bf16 pairs; row sum in fp32 (four packed chains)
+        if constexpr (C::kTurns) {
+          if (!take_turn()) return false;
+        }
         const uint64_t sl2v = pack_f32x2(sl2, sl2), negm = pack_f32x2(-msub, -msub);
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[64];
@@ -567,6 +618,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         const float2 c0 = unpack_f32x2(acc[0]), c1 = unpack_f32x2(acc[1]);
         const float2 c2 = unpack_f32x2(acc[2]), c3 = unpack_f32x2(acc[3]);
         l += ((c0.x + c0.y) + (c1.x + c1.y)) + ((c2.x + c2.y) + (c3.x + c3.y));
+        if constexpr (C::kTurns) {
+          pass_turn();
+          ++taken;
+        }
         if (!C::kSepP) {  // P over S_t: every S value is already in registers
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * c]));
@@ -605,6 +660,13 @@ __global__ void __launch_bounds__(kK1Threads, 1)
                                        r == 0 ? T.itm.kv[0].len : T.itm.kv[1].len, qa_t, qb_t, p);
         for (int j = R.lo; j <= R.hi && ok; ++j)
           ok = step(j >= R.flo && j <= R.fhi, R.kpos0 + j * kBlockN, min(kBlockN, R.len - j * kBlockN));
+      }
+      // the other tile's extra steps: pass the turns before this tile's epilogue
+      if constexpr (C::kTurns) {
+        for (; taken < n_turns && ok; ++taken) {
+          ok = take_turn();
+          if (ok) pass_turn();
+        }
       }
       if (!ok) break;
 
