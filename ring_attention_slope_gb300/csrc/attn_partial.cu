@@ -75,7 +75,9 @@ struct K1Cfg {
   static constexpr int kStageBufs = kStageOffset + 2 * 4 * kQTiles * 4096 + 2048 <= 232448 ? 2 : 1;
   static constexpr int kStageBytes = kStageBufs * 4 * kQTiles * 4096;
   static constexpr int kBarOffset = kStageOffset + kStageBytes;
-  static constexpr int kSmemBytes = 1024 + kBarOffset + 8 * kNumBars + 16;
+  // the launch's work items, copied from the kernel parameters (read on every work tile)
+  static constexpr int kItemsOffset = kBarOffset + ((8 * kNumBars + 16 + 15) / 16) * 16;
+  static constexpr int kSmemBytes = 1024 + kItemsOffset + kMaxItems * static_cast<int>(sizeof(WorkItem));
   static constexpr uint32_t kColO = 256;
   static constexpr uint32_t kColP = kColO + kQTiles * DV;           // separate P columns, if they fit
   static constexpr bool kSepP = kColP + kQTiles * (kBlockN / 2) <= 512;
@@ -201,9 +203,9 @@ struct Tile {
 // later (heavier under the causal mask) row blocks before its earlier ones.
 // `ii` carries the item index from the caller's previous work tile: a CTA visits its
 // tiles in increasing w, so the item index never decreases and the scan resumes there.
-__device__ __forceinline__ void decode_tile(const AttnParams& p, int w, Tile& T, int& ii) {
-  while (ii < p.n_items - 1 && w >= (p.items[ii].cta_begin + p.items[ii].n_blocks) * p.Hq) ++ii;
-  T.itm = p.items[ii];
+__device__ __forceinline__ void decode_tile(const AttnParams& p, const WorkItem* items, int w, Tile& T, int& ii) {
+  while (ii < p.n_items - 1 && w >= (items[ii].cta_begin + items[ii].n_blocks) * p.Hq) ++ii;
+  T.itm = items[ii];
   const int local = w - T.itm.cta_begin * p.Hq;
   T.blk = T.itm.n_blocks - 1 - local / p.Hq;
   T.h = local % p.Hq;
@@ -273,6 +275,14 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     }
     fence_barrier_init();
   }
+  // work items into shared memory: dynamically indexed parameter reads miss the constant cache
+  WorkItem* sItems = reinterpret_cast<WorkItem*>(smem + C::kItemsOffset);
+  {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(p.items);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(sItems);
+    const int words = p.n_items * static_cast<int>(sizeof(WorkItem) / 4);
+    for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+  }
   if (threadIdx.x == kTmaWarp * 32) {
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
@@ -293,7 +303,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       int item_hint = 0;
       for (int w = blockIdx.x; w < total; w += gridDim.x) {
         Tile T;
-        decode_tile(p, w, T, item_hint);
+        decode_tile(p, sItems, w, T, item_hint);
         if (!has_steps(T.itm, p, T.geo)) continue;
         // Q of the previous work tile is in use until its last S MMAs are done
         if (wt > 0 && !wait_bounded(bar_qempty, (wt - 1) & 1, cta_abort, p.status, limit, 11)) {
@@ -409,7 +419,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       int item_hint = 0;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         Tile T;
-        decode_tile(p, w, T, item_hint);
+        decode_tile(p, sItems, w, T, item_hint);
         if (!has_steps(T.itm, p, T.geo)) continue;
         if (!wait_bounded(bar_q, wt & 1, cta_abort, p.status, limit, 3)) {
           ok = false;
@@ -507,7 +517,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     int item_hint = 0;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       Tile T;
-      decode_tile(p, w, T, item_hint);
+      decode_tile(p, sItems, w, T, item_hint);
       const int rows_t = t == 0 ? T.geo.rows[0] : T.geo.rows[1];
       // turns of this work tile: the step count of the tile with more steps
       int n_turns = 0;

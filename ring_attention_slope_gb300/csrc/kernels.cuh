@@ -33,6 +33,7 @@ struct WorkItem {
   int32_t n_blocks;   // ceil(q_len / kRowsPerCta)
   KvRange kv[kMaxKvRanges];
 };
+static_assert(sizeof(WorkItem) % 4 == 0, "work items are copied as 32-bit words");
 
 struct AttnParams {
   int32_t n_items;
