@@ -310,6 +310,9 @@ def run_gpu(args, w):
     merge_bytes = merge_bytes_per_launch(slope, w, n, sizes, window)
     k2_gbs = merge_bytes * k2_n / (k2_ms * 1e-3) / 1e9 if k2_ms > 0 else None
 
+    # ---- the same attention as one launch (bf16 out, no partials, no merge): the fused single-GPU form
+    fused = run_fused(slope, torch, w, window, q, k, v, stream, args, barrier, dist)
+
     # ---- end to end through the public call with pinned host buffers
     e2e = None if args.no_e2e else run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier,
                                            dist)
@@ -338,6 +341,7 @@ def run_gpu(args, w):
                            "bytes_per_launch": merge_bytes, "kernel": "lse_merge_kernel",
                            "avg_launch_ms": k2_ms / max(1, k2_n)},
         "e2e": e2e,
+        "fused_single_launch": fused,
         "gpu_launches": int(sum(counts)),
         "clocks": clocks,
     }
@@ -378,6 +382,32 @@ def merge_bytes_per_launch(slope, w, n, sizes, window):
         live_rows[it["plane"]] += int(seen.sum())
     reads = int(plane_live.sum()) * w.S * 4 + int(live_rows[plane_live].sum()) * w.dv * 4
     return float(w.Hq * (reads + w.S * (w.dv * 2 + 4)))
+
+
+def run_fused(slope, torch, w, window, q, k, v, stream, args, barrier, dist):
+    """The whole causal attention as one attention launch over the full sequence (bf16 out): every query
+    tile runs the online softmax over all of its visible keys, with no partials and no merge."""
+    out = torch.empty((w.S, w.Hq, w.dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.Hq, w.S), dtype=torch.float32, device="cuda")
+
+    def step():
+        slope.attn_partial(q, k, v, causal=True, window=window, out=out, lse=lse)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), dist, "cuda")
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": job_tflops(workload_flops(w, window), args.steps, world, ms), "unit": UNIT,
+            "ms_per_step": ms / args.steps, "api": "slope_attn_partial over the whole sequence, bf16 out",
+            "gpu_launches_per_step": 1}
 
 
 def run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier, dist):

@@ -97,9 +97,14 @@ typedef enum {
  *   q   bf16 [Sq, Hq, dqk]    k bf16 [Skv, Hkv, dqk]    v bf16 [Skv, Hkv, dv]
  *   q_off / kv_off: global positions of q row 0 / k row 0 (the masks use them).
  *   causal, window, scale: see the conventions above.
- *   out fp32 [Sq, Hq, dv]: the softmax-normalised output over the visible keys
- *       of this block (0 for rows that see none).  Innermost stride 1, row and
- *       head strides multiples of 4 elements, pointer 16-byte aligned.
+ *   out fp32 or bf16 [Sq, Hq, dv]: the softmax-normalised output over the
+ *       visible keys of this block (0 for rows that see none).  Innermost
+ *       stride 1, pointer 16-byte aligned; row and head strides multiples of
+ *       4 elements (fp32) or 8 elements (bf16).  With q, k and v covering the
+ *       whole sequence (q_off = kv_off = 0) and bf16 out, this one launch is
+ *       the whole attention: every query tile runs the online softmax over
+ *       all of its visible keys, with no partials and no merge (the fused
+ *       single-GPU form of the ring).
  *   lse fp32, rank 2 [Hq, Sq] (any strides): natural-log log-sum-exp of the
  *       scaled scores over the visible keys of this block (-inf if none).
  * Sq == 0 is a no-op.  Returns SLOPE_OK or an error status.

@@ -177,16 +177,17 @@ def _layout(layout):
 # ---------------------------------------------------------------- public calls
 
 def attn_partial(q, k, v, *, q_off=0, kv_off=0, causal=True, window=0, scale=0.0, out=None, lse=None,
-                 stream=None):
+                 out_dtype=None, stream=None):
     """Partial attention of q [Sq,Hq,dqk] against k [Skv,Hkv,dqk], v [Skv,Hkv,dv] (bf16, CUDA).
 
-    Returns ``(out, lse)``: out fp32 [Sq,Hq,dv], lse fp32 [Hq,Sq] (natural log).
+    Returns ``(out, lse)``: out fp32 (default) or bf16 [Sq,Hq,dv], lse fp32 [Hq,Sq] (natural log).
+    Over the whole sequence with bf16 out this is the whole attention in one launch.
     """
     torch = _torch()
     Sq, Hq, _ = q.shape
     dv = v.shape[2]
     if out is None:
-        out = torch.empty((Sq, Hq, dv), dtype=torch.float32, device=q.device)
+        out = torch.empty((Sq, Hq, dv), dtype=out_dtype or torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((Hq, Sq), dtype=torch.float32, device=q.device)
     dq, dk, dvv, do, dl = _desc(q), _desc(k), _desc(v), _desc(out), _desc(lse)

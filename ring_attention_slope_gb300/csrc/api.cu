@@ -124,20 +124,23 @@ bool make_map(CUtensorMap* m, const slope_tensor* t) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D view {dv, H, rows} of an fp32 output with row/head strides in elements; box = 32
-// columns x 1 head x 32 rows (one softmax warp's rows), 128-byte swizzle, written by TMA
-// stores from the attention kernel's epilogue.  Returns false if the map cannot be built
-// (the kernel then stores directly).
-bool make_out_map(CUtensorMap* m, float* base, int64_t rows, int64_t H, int64_t dv, int64_t srow, int64_t shead) {
+// 3-D view {dv, H, rows} of an fp32 or bf16 output with row/head strides in elements;
+// box = 128 bytes of columns (32 fp32 or 64 bf16) x 1 head x 32 rows (one softmax warp's
+// rows), 128-byte swizzle, written by TMA stores from the attention kernel's epilogue.
+// Returns false if the map cannot be built (the kernel then stores directly).
+bool make_out_map(CUtensorMap* m, void* base, bool bf16, int64_t rows, int64_t H, int64_t dv, int64_t srow,
+                  int64_t shead) {
   auto enc = encode_fn();
   if (enc == nullptr || rows <= 0 || rows > 0x7fffffffLL) return false;
+  const cuuint64_t esize = bf16 ? 2 : 4;
+  if ((srow * esize) % 16 != 0 || (shead * esize) % 16 != 0 || !aligned(base, 16)) return false;
   std::memset(m, 0, sizeof(*m));
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(dv), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(shead) * 4, static_cast<cuuint64_t>(srow) * 4};
-  cuuint32_t box[3] = {32, 1, 32};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(shead) * esize, static_cast<cuuint64_t>(srow) * esize};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), 1, 32};
   cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -413,7 +416,9 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   base.wait_limit_ns = wait_limit_ns();
   CUtensorMap to;
   base.out_plane_rows = S;
-  base.out_tma = make_out_map(&to, planes, static_cast<int64_t>(plan.n_planes) * S, Hq, dv, Hq * dv, dv) ? 1 : 0;
+  base.out_bf16 = 0;
+  base.out_tma =
+      make_out_map(&to, planes, false, static_cast<int64_t>(plan.n_planes) * S, Hq, dv, Hq * dv, dv) ? 1 : 0;
   if (!base.out_tma) to = tq;  // never used
 
   // A plane none of whose items sees a key (ring steps that a sliding window leaves
@@ -601,7 +606,10 @@ slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, co
   if (!attn_partial_supported(static_cast<int>(dqk), static_cast<int>(dv))) return SLOPE_ERR_UNSUPPORTED;
   if (window < 0 || window > kMaxSeq) return SLOPE_ERR_SHAPE;
   if (std::llabs(q_off) > kMaxSeq || std::llabs(kv_off) > kMaxSeq) return SLOPE_ERR_SHAPE;
-  if ((st = check_out(out, Sq, Hq, dv, false)) != SLOPE_OK) return st;
+  if ((st = check_out(out, Sq, Hq, dv, true)) != SLOPE_OK) return st;
+  // bf16 rows are written 16 bytes at a time
+  if (out->dtype == SLOPE_BF16 && (out->stride[0] % 8 || out->stride[1] % 8 || !aligned(out->data, 16)))
+    return SLOPE_ERR_STRIDE;
   if ((st = check_lse(lse, Hq, Sq)) != SLOPE_OK) return st;
   if (Sq == 0) return SLOPE_OK;
   int* status = device_status_ptr();
@@ -649,7 +657,8 @@ slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, co
   base.wait_limit_ns = wait_limit_ns();
   CUtensorMap to;
   base.out_plane_rows = 0;
-  base.out_tma = make_out_map(&to, base.out, Sq, Hq, dv, out->stride[0], out->stride[1]) ? 1 : 0;
+  base.out_bf16 = out->dtype == SLOPE_BF16 ? 1 : 0;
+  base.out_tma = make_out_map(&to, out->data, base.out_bf16 != 0, Sq, Hq, dv, out->stride[0], out->stride[1]) ? 1 : 0;
   if (!base.out_tma) to = tq;  // never used
   return run_attention(groups[0], static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, to, base, nullptr,
                        static_cast<cudaStream_t>(stream));

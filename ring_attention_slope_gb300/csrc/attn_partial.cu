@@ -28,6 +28,8 @@
 // running max is only moved when it grows by more than 8 (factor 256), which
 // keeps every p <= 256 and makes most O rescales unnecessary; the final
 // normalisation uses the same max, so the result is exact either way.
+#include <cuda_bf16.h>
+
 #include <algorithm>
 
 #include "kernels.cuh"
@@ -696,54 +698,115 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         // a row that saw no key keeps m = -inf; its l holds only the clamped 2^-125
         // terms of the polynomial pairs, and its output is 0
         const float inv = (l > 0.f && m_used > -INFINITY) ? 1.f / l : 0.f;
+        if (p.out_bf16) {
+          // bf16 output: two 32-column TMEM loads fill one 64-column (128-byte) box row
+          __nv_bfloat16* bp = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                              (static_cast<int64_t>(T.itm.plane) * p.out_splane + orow * p.out_srow +
+                               static_cast<int64_t>(T.h) * p.out_shead);
 #pragma unroll
-        for (int c = 0; c < DV / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait();
-          reg_fence(o);
-          if (c == DV / 32 - 1) {  // O_t is read: the next work tile's first PV may overwrite it
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_ofree[t]);
+          for (int g = 0; g < DV / 64; ++g) {
+            uint32_t wv[32];
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+              const int c = 2 * g + hlf;
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_ld_wait();
+              reg_fence(o);
+              if (c == DV / 32 - 1) {  // O_t is read: the next work tile's first PV may overwrite it
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_ofree[t]);
+              }
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                wv[16 * hlf + i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+            }
+            if (via_tma) {
+              uint8_t* const box = sStage + (g % C::kStageBufs) * 4096;
+              if (lane == 0) {
+                if (C::kStageBufs == 2)
+                  bulk_wait_read_allbut1();
+                else
+                  bulk_wait_read_all();
+              }
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<uint4*>(box + lane * 128 + ((i ^ (lane & 7)) * 16)) =
+                    make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+              fence_proxy_async_shared();
+              __syncwarp();
+              if (lane == 0) {
+                const int64_t z = static_cast<int64_t>(T.itm.plane) * p.out_plane_rows + orow;  // row of lane 0
+                tma_store_3d(&tm_o, box, 64 * g, T.h, static_cast<int>(z));
+                bulk_commit();
+              }
+            } else if (valid_row) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<uint4*>(bp + 64 * g + 8 * i) =
+                    make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+            }
           }
-          if (via_tma) {
-            uint8_t* const box = sStage + (c % C::kStageBufs) * 4096;
-            // the store that last used this box has read it (with two boxes the most
-            // recent store, into the other box, may still be reading)
-            if (lane == 0) {
-              if (C::kStageBufs == 2)
-                bulk_wait_read_allbut1();
-              else
-                bulk_wait_read_all();
-            }
-            __syncwarp();
-            // row `lane` of the box: 16-byte chunk i at chunk position i ^ (lane & 7) (128-byte swizzle)
+        } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                           __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-              *reinterpret_cast<float4*>(box + lane * 128 + ((i ^ (lane & 7)) * 16)) = v;
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+            reg_fence(o);
+            if (c == DV / 32 - 1) {  // O_t is read: the next work tile's first PV may overwrite it
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bar_ofree[t]);
             }
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              const int64_t z = static_cast<int64_t>(T.itm.plane) * p.out_plane_rows + orow;  // row of lane 0
-              tma_store_3d(&tm_o, box, 32 * c, T.h, static_cast<int>(z));
-              bulk_commit();
-            }
-          } else if (valid_row) {
+            if (via_tma) {
+              uint8_t* const box = sStage + (c % C::kStageBufs) * 4096;
+              // the store that last used this box has read it (with two boxes the most
+              // recent store, into the other box, may still be reading)
+              if (lane == 0) {
+                if (C::kStageBufs == 2)
+                  bulk_wait_read_allbut1();
+                else
+                  bulk_wait_read_all();
+              }
+              __syncwarp();
+              // row `lane` of the box: 16-byte chunk i at chunk position i ^ (lane & 7) (128-byte swizzle)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                     __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-              *reinterpret_cast<float4*>(op + c * 32 + 4 * i) = v;
+              for (int i = 0; i < 8; ++i) {
+                const float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                             __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+                *reinterpret_cast<float4*>(box + lane * 128 + ((i ^ (lane & 7)) * 16)) = v;
+              }
+              fence_proxy_async_shared();
+              __syncwarp();
+              if (lane == 0) {
+                const int64_t z = static_cast<int64_t>(T.itm.plane) * p.out_plane_rows + orow;  // row of lane 0
+                tma_store_3d(&tm_o, box, 32 * c, T.h, static_cast<int>(z));
+                bulk_commit();
+              }
+            } else if (valid_row) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                       __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+                *reinterpret_cast<float4*>(op + c * 32 + 4 * i) = v;
+              }
             }
           }
         }
       } else if (p.write_empty_out && valid_row) {
+        if (p.out_bf16) {
+          __nv_bfloat16* bp = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                              (static_cast<int64_t>(T.itm.plane) * p.out_splane + orow * p.out_srow +
+                               static_cast<int64_t>(T.h) * p.out_shead);
 #pragma unroll
-        for (int i = 0; i < DV / 4; ++i) *reinterpret_cast<float4*>(op + 4 * i) = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int i = 0; i < DV / 8; ++i) *reinterpret_cast<uint4*>(bp + 8 * i) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+#pragma unroll
+          for (int i = 0; i < DV / 4; ++i) *reinterpret_cast<float4*>(op + 4 * i) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
       if (valid_row) {
         p.lse[static_cast<int64_t>(T.itm.plane) * p.lse_splane + orow * p.lse_srow +

@@ -46,8 +46,9 @@ struct AttnParams {
   int32_t kv_pos_off;       // global position of k row 0
   int32_t write_empty_out;  // write zeros to out for rows that see no key
   float scale_log2;         // softmax scale * log2(e)
-  float* out;               // fp32 partial output planes
-  int64_t out_srow, out_shead, out_splane;
+  float* out;               // output planes: fp32 partials, or bf16 when out_bf16
+  int64_t out_srow, out_shead, out_splane;  // in elements
+  int32_t out_bf16;         // 1: out holds bf16 (a final output, not a partial)
   int32_t out_tma;          // 1: full 32-row warp chunks of out go through the O tensor map
   int64_t out_plane_rows;   // rows per plane in the O tensor map's outer dimension
   float* lse;               // fp32 log-sum-exp planes

@@ -93,7 +93,8 @@ def test_attn_partial_and_merge_argument_errors(lib):
         return lib.slope_attn_partial(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 0, 0, 1, 0, 0.0,
                                       ctypes.byref(out) if out else None, ctypes.byref(lse) if lse else None, None)
 
-    assert call(out=_t([Sq, Hq, 64], dtype=0)) == E_DTYPE      # partial out must be fp32
+    assert call(out=_t([Sq, Hq, 64], dtype=5)) == E_DTYPE      # unknown dtype
+    assert call(out=_t([Sq, Hq, 64], dtype=0, stride=[Hq * 64 + 4, 64, 1])) == E_STRIDE  # bf16 row: 8 elements
     assert call(lse=None) == E_NULL
     assert call(v=_t([Skv, Hkv, 192])) == E_UNSUP              # (128, 192)
     assert call(k=_t([Skv + 1, Hkv, d])) == E_SHAPE

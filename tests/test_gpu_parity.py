@@ -326,3 +326,36 @@ def test_cp_prefill_host_buffers_overlapped_calls(layout, n):
         assert torch.equal(houts[i], ro.cpu()), f"call {i}: out differs"
         assert torch.equal(hlses[i], rl.cpu()), f"call {i}: lse differs"
     assert slope.device_status() == (0, 0)
+
+
+@pytest.mark.parametrize("Sq,Hq,Hkv,d,window", [(1000, 8, 2, 64, 0), (777, 4, 4, 64, 100), (640, 4, 4, 128, 0)])
+def test_attn_partial_bf16_out_is_the_fp32_out_rounded(Sq, Hq, Hkv, d, window):
+    """bf16 output: the same normalised rows as the fp32 output, rounded to bf16 (same kernel arithmetic),
+    including rows of ragged 32-row chunks that are stored directly."""
+    q, k, v = qkv(Sq, Hq, Hkv, d, d, seed=Sq + d)
+    o32, l32 = slope.attn_partial(q, k, v, causal=True, window=window)
+    o16, l16 = slope.attn_partial(q, k, v, causal=True, window=window, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert o16.dtype == torch.bfloat16
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.equal(l16, l32)
+    assert slope.device_status() == (0, 0)
+
+
+@pytest.mark.parametrize("layout,n", [("zigzag", 8), ("chunked", 3)])
+def test_fused_single_launch_matches_ring_and_oracle(layout, n):
+    """The whole causal attention in one attention launch (bf16 out, no partials, no merge) agrees with
+    the ring / chunked decomposition and with the oracle on sampled rows."""
+    S, Hq, Hkv, d = 4096, 8, 2, 64
+    q, k, v = qkv(S, Hq, Hkv, d, d, seed=123, scale_v=0.5)
+    fo, fl = slope.attn_partial(q, k, v, causal=True, out_dtype=torch.bfloat16)
+    ro, rl = slope.cp_prefill(q, k, v, n, layout)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([np.arange(0, 130), np.arange(S - 130, S),
+                                     np.random.default_rng(5).integers(0, S, 600)]))
+    oo, ol = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, rows=rows)
+    compare(fo.float().cpu()[rows], fl.cpu()[:, rows], oo, ol, f"fused vs oracle ({layout})")
+    d_out = (fo.float() - ro.float()).abs().max().item()
+    d_lse = (fl - rl).abs().max().item()
+    assert d_out <= 2e-2 and d_lse <= 1e-3, (d_out, d_lse)
+    assert slope.device_status() == (0, 0)
