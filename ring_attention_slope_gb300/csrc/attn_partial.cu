@@ -622,11 +622,31 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[64];
         const Exp2Poly poly = exp2_poly_consts();
+        // P is stored in 16-column chunks while later pairs are still being exponentiated.
+        // Over S_t (dv = 128) each chunk goes out when done; in its own columns (dv = 64) the
+        // previous PV must have read P first, which it has by three quarters of the loop.
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
+        for (int i = 0; i < 64; ++i) {
           pk[i] = (i & 15) < kPolyPairsPer16
                       ? softmax_pair_poly(sv[2 * i], sv[2 * i + 1], sl2v, negm, acc[i & 3], poly)
                       : softmax_pair(sv[2 * i], sv[2 * i + 1], sl2v, negm, acc[i & 3]);
+          if ((i & 15) == 15) {
+            const int c = i >> 4;  // chunk c of P is complete
+            if constexpr (!C::kSepP) {
+              tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * c]));
+            } else if (c == 2) {
+              if (n > 0) {
+                if (!warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 9))) return false;
+                tc_fence_after_sync();
+              }
+#pragma unroll
+              for (int cc = 0; cc < 3; ++cc)
+                tmem_st16(tP + cc * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * cc]));
+            } else if (c == 3) {
+              tmem_st16(tP + 48, *reinterpret_cast<const uint32_t(*)[16]>(&pk[48]));
+            }
+          }
+        }
         const float2 c0 = unpack_f32x2(acc[0]), c1 = unpack_f32x2(acc[1]);
         const float2 c2 = unpack_f32x2(acc[2]), c3 = unpack_f32x2(acc[3]);
         l += ((c0.x + c0.y) + (c1.x + c1.y)) + ((c2.x + c2.y) + (c3.x + c3.y));
@@ -634,18 +654,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           pass_turn();
           ++taken;
         }
-        if (!C::kSepP) {  // P over S_t: every S value is already in registers
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * c]));
-        }
-        if ((C::kSepP && n > 0) || (any_need && nl > 0)) {
-          // the previous PV of this tile must be done before P_t is overwritten / O_t is rescaled
+        if (!C::kSepP && any_need && nl > 0) {
+          // the previous PV of this tile must be done before O_t is rescaled
           if (!warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 9))) return false;
           tc_fence_after_sync();
-        }
-        if (C::kSepP) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_st16(tP + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * c]));
         }
         if (any_need && nl > 0) {
 #pragma unroll 1
