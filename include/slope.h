@@ -134,16 +134,19 @@ SLOPE_API slope_status slope_lse_merge(const slope_tensor* outs, const slope_ten
  *   q bf16 [S, Hq, dqk], k bf16 [S, Hkv, dqk], v bf16 [S, Hkv, dv] (positions 0..S-1).
  *   layout SLOPE_LAYOUT_CONTIGUOUS / SLOPE_LAYOUT_ZIGZAG: a ring of n_chunks
  *     simulated ranks.  At ring step t rank r holds the keys/values of rank
- *     (r - t) mod n_chunks; each step is ONE attention-kernel launch covering
- *     every rank, writing one partial per (rank, step); a final merge launch
- *     combines each row's partials.  A step in which no query sees any key
- *     (possible only with a window) is skipped, and so is its partial in the
- *     merge.  CONTIGUOUS needs S % n_chunks == 0,
+ *     (r - t) mod n_chunks; every step computes one partial per (rank, step),
+ *     and a final merge launch combines each row's partials.  Steps run in
+ *     order, consecutive steps sharing an attention-kernel launch up to 32
+ *     work items (two per rank and step in ZIGZAG, one in CONTIGUOUS); each
+ *     partial is the same as in a launch of its own.  A step in which no query
+ *     sees any key (possible only with a window) is skipped, and so is its
+ *     partial in the merge.  CONTIGUOUS needs S % n_chunks == 0,
  *     ZIGZAG needs S % (2*n_chunks) == 0.  1 <= n_chunks <= 32.
  *   layout SLOPE_LAYOUT_CHUNKED: n_chunks query chunks, sizes chunk_sizes[0..n)
  *     (summing to S), or NULL for ceil(S/n_chunks) with a shorter last chunk.
  *     Chunk [s, e) yields two partials - against keys [0, s) and, causally,
- *     against [s, e) - computed in one launch per chunk, in order, then merged.
+ *     against [s, e) - computed chunk by chunk, in order (consecutive chunks
+ *     sharing a launch up to 32 work items), then merged.
  *   causal, window, scale: as above.  out: bf16 or fp32 [S, Hq, dv];
  *   lse: fp32 [Hq, S] or NULL.
  *   workspace: device buffer of at least slope_cp_prefill_workspace_size()

@@ -430,13 +430,23 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   for (const PItem& it : plan.items)
     if (it.n_kv > 0) plane_live[static_cast<size_t>(it.plane)] = 1;
 
-  // One or more launches per ring step / chunk, in order.
+  // Ring steps / chunks in order.  Their partials are independent of each other on one GPU
+  // (every step reads only the inputs and writes its own plane), so consecutive steps share
+  // a kernel launch up to the launch's item limit: each partial is computed by the same code
+  // as in a launch of its own, with fewer launch prologues and tails.
   size_t i = 0;
   std::vector<std::vector<WorkItem>> groups;
-  for (int l = 0; l < plan.n_launches; ++l) {
+  for (int l = 0; l < plan.n_launches;) {
     std::vector<PItem> items;
-    for (; i < plan.items.size() && plan.items[i].launch == l; ++i)
-      if (plane_live[static_cast<size_t>(plan.items[i].plane)]) items.push_back(plan.items[i]);
+    for (; l < plan.n_launches; ++l) {
+      std::vector<PItem> step_items;
+      size_t j = i;
+      for (; j < plan.items.size() && plan.items[j].launch == l; ++j)
+        if (plane_live[static_cast<size_t>(plan.items[j].plane)]) step_items.push_back(plan.items[j]);
+      if (!items.empty() && items.size() + step_items.size() > static_cast<size_t>(kMaxItems)) break;
+      items.insert(items.end(), step_items.begin(), step_items.end());
+      i = j;
+    }
     if (items.empty()) continue;
     pack_items(items, causal, groups);
     for (const auto& g : groups)

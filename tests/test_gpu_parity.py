@@ -219,7 +219,8 @@ def test_cp_prefill_skips_ring_steps_without_keys():
     events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_steps + 1)]
     out, lse, n_launches, kinds = slope.cp_prefill_timed(q, k, v, N, "zigzag", events, window=W)
     torch.cuda.synchronize()
-    assert kinds.count(0) == len(live) and kinds.count(1) == 1 and n_launches == len(live) + 1
+    # consecutive live steps share a launch up to 32 work items: steps 0 and 1 (16 items each), then step 7
+    assert kinds.count(0) == 2 and kinds.count(1) == 1 and n_launches == 3
     ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, window=W)
     compare(out.float().cpu(), lse.cpu(), ro, rl, "zigzag-8 window 100")
     assert slope.device_status() == (0, 0)
