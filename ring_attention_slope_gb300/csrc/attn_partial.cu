@@ -585,12 +585,15 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         }
         float mx = fmax3(q0, q1, fmaxf(q2, q3));  // row max of a fully visible tile
         if (!full) {
+          // the row's visible columns of this tile form one interval [lo, hi]: c < valid,
+          // causal kpos + c <= q_pos, window q_pos - (kpos + c) < window
+          int lo = p.window > 0 ? max(0, q_pos - kpos - p.window + 1) : 0;
+          int hi = p.causal ? min(valid - 1, q_pos - kpos) : valid - 1;
+          if (hi < lo) lo = hi = kBlockN;  // nothing visible: every c - lo is negative
+          const uint32_t span = static_cast<uint32_t>(hi - lo);
 #pragma unroll
-          for (int c = 0; c < kBlockN; ++c) {
-            const int kp = kpos + c;
-            const bool vis = c < valid && (!p.causal || kp <= q_pos) && (p.window == 0 || q_pos - kp < p.window);
-            if (!vis) sv[c] = -INFINITY;
-          }
+          for (int c = 0; c < kBlockN; ++c)
+            if (static_cast<uint32_t>(c - lo) > span) sv[c] = -INFINITY;
           // row max over the visible scores: four independent chains of 3-input max
           float a0 = sv[0], a1 = sv[1], a2 = sv[2], a3 = sv[3];
 #pragma unroll
