@@ -360,3 +360,31 @@ def test_fused_single_launch_matches_ring_and_oracle(layout, n):
     d_lse = (fl - rl).abs().max().item()
     assert d_out <= 2e-2 and d_lse <= 1e-3, (d_out, d_lse)
     assert slope.device_status() == (0, 0)
+
+
+def test_cp_prefill_host_more_buffer_sets_than_tracked():
+    """18 device-buffer sets in rotation (the library tracks 16: older sets are waited for and their
+    slots reused), the first set reused at the end, and no lse: every result equals cp_prefill."""
+    S, Hq, Hkv, d, n = 512, 4, 1, 64, 2
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    sets = [dict(q=torch.empty(S, Hq, d, dtype=torch.bfloat16, device="cuda"),
+                 k=torch.empty(S, Hkv, d, dtype=torch.bfloat16, device="cuda"),
+                 v=torch.empty(S, Hkv, d, dtype=torch.bfloat16, device="cuda"),
+                 out=torch.empty(S, Hq, d, dtype=torch.bfloat16, device="cuda")) for _ in range(18)]
+    order = list(range(18)) + [0, 1]
+    inputs, outs = [], []
+    ws = None
+    for j, i in enumerate(order):
+        hq, hk, hv = (t.pin_memory() for t in qkv(S, Hq, Hkv, d, d, seed=300 + j, device="cpu"))
+        ho = torch.empty(S, Hq, d, dtype=torch.bfloat16).pin_memory()
+        b = sets[i]
+        ws = slope.cp_prefill_host(hq, hk, hv, ho, None, b["q"], b["k"], b["v"], b["out"], None, n, "zigzag",
+                                   workspace=ws, copy_in_stream=s_in, compute_stream=s_c, copy_out_stream=s_out)
+        inputs.append((hq, hk, hv))
+        outs.append(ho)
+    torch.cuda.synchronize()
+    for j in range(len(order)):
+        ro, _ = slope.cp_prefill(*(t.cuda() for t in inputs[j]), n, "zigzag", want_lse=False)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[j], ro.cpu()), f"call {j} (buffer set {order[j]})"
+    assert slope.device_status() == (0, 0)
