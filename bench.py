@@ -1,18 +1,20 @@
 """Benchmark: context-parallel causal GQA prefill attention on GB300.
 
 One step = one ``slope_cp_prefill`` call over the whole workload: every ring
-step's attention launch (partial output + log-sum-exp per rank) followed by
-the exact log-sum-exp merge.  Default workload: S = 32768, 64 query / 8 KV
-heads, head dim 64, bf16, zigzag ring of 8 simulated ranks.
+step's partial (output + log-sum-exp per rank and step) followed by the exact
+log-sum-exp merge.  Default workload: S = 32768, 64 query / 8 KV heads, head
+dim 64, bf16, zigzag ring of 8 simulated ranks.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--window W] [--impl reference]
 
 Prints one JSON line (rank 0).  ``value`` is algorithmic TFLOP/s (visible
-query-key pairs x Hq x 2 x (dqk + dv)) of the whole job; ``e2e`` is the same
-metric measured through the public call with pinned host buffers (host to
-device copies of Q/K/V and device to host copies of out/lse inside the timed
-region).  ``--impl reference`` times the fp64 CPU oracle on a bounded sample
-of the same workload (rank 0 only).
+query-key pairs x Hq x 2 x (dqk + dv)) of the whole job.  ``e2e`` is the same
+metric through ``slope_cp_prefill_host`` with pinned host buffers: every step
+copies Q/K/V in and out/lse back inside the timed region, two device-buffer
+sets letting each step's copies overlap its neighbours' compute.
+``fused_single_launch`` is the same attention as one launch over the whole
+sequence (no partials, no merge).  ``--impl reference`` times the fp64 CPU
+oracle on a bounded sample of the same workload (rank 0 only).
 """
 from __future__ import annotations
 

@@ -1,4 +1,5 @@
-// Partial attention kernel (one ring step / one chunked-prefill launch).
+// Partial attention kernel (ring steps / chunked-prefill chunks, or the whole
+// sequence in one launch).
 //
 // Computes, for every work item (a block of query rows and up to two
 // key/value row ranges), softmax attention restricted to the visible keys of
@@ -6,15 +7,17 @@
 // log-sum-exp: the per-device partial of Ring Attention (Moreh, "Optimizing
 // long-context prefill on multiple older-generation GPU nodes", section
 // "Introduction to Context Parallelism", Ring Attention item), combined later
-// by the log-sum-exp merge.
+// by the log-sum-exp merge.  Over the whole sequence with bf16 output the same
+// launch is the complete attention (no partials, no merge).
 //
-// Structure (one CTA = one item x 256 query rows x one query head):
+// Persistent grid: one CTA per SM walks work tiles (one item x 256 query rows x
+// one query head), heaviest first; the launch's items sit in shared memory.
 //   warps 0-3   online softmax of Q tile 0 (one query row per thread = TMEM lane),
 //   warps 4-7   online softmax of Q tile 1; each also runs its tile's epilogue,
-//               which stages O in shared memory (a 32 x 32 fp32 box per warp)
-//               and writes it with TMA stores.
-//   warp 8      TMA producer: Q tiles once, then K and V tiles through a ring
-//               of shared-memory slots (128-byte swizzle, 64-column chunks).
+//               which stages O in shared memory (32-row x 128-byte boxes per
+//               warp, fp32 or bf16) and writes it with TMA stores.
+//   warp 8      TMA producer: Q tiles once per work tile, then K and V tiles
+//               through a ring of shared-memory slots (128-byte swizzle).
 //   warps 9-10  MMA issuers, one per Q tile: S_t = Q_t K^T (SS, K-major) into
 //               TMEM, then O_t += P_t V (P from TMEM, V MN-major); warp 9 also
 //               owns the 512-column TMEM allocation.
@@ -23,11 +26,14 @@
 // With dv = 64 the last 128 columns hold P_0 and P_1 (bf16 pairs, 64 columns
 // each), so the MMA warp issues S(n+1) = Q K(n+1)^T before O += P(n) V(n) and
 // the softmax of step n+1 starts while PV(n) still runs.  With dv = 128 TMEM is
-// full: P_t overwrites the first 64 columns of S_t, and S(n+1) waits for PV(n).
-// Scores live in the log2 domain (scale * log2 e folded into one FMA); the
-// running max is only moved when it grows by more than 8 (factor 256), which
-// keeps every p <= 256 and makes most O rescales unnecessary; the final
-// normalisation uses the same max, so the result is exact either way.
+// full: P_t overwrites the first 64 columns of S_t, S(n+1) waits for PV(n), and
+// the two softmax warps of each SM sub-partition take turns on the exponentials.
+// The load of S returns each 32-column quarter's maximum (tcgen05.ld.red), which
+// is the row max of a fully visible tile.  Scores live in the log2 domain
+// (scale * log2 e folded into one FMA); the running max is only moved when it
+// grows by more than 8 (factor 256), which keeps every p <= 256 and makes most O
+// rescales unnecessary; the final normalisation uses the same max, so the
+// result is exact either way.
 #include <cuda_bf16.h>
 
 #include <algorithm>
