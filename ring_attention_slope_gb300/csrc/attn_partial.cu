@@ -615,13 +615,11 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         }
         const float m_new = mx * sl2;
         const bool need = m_new > m_used + kRescaleThreshold;
-        const bool any_need = __any_sync(0xffffffffu, need);
-        float alpha = 1.f;
-        if (need) {
-          alpha = ex2_approx(m_used - m_new);
-          m_used = m_new;
-          l *= alpha;
-        }
+        // per-lane update without a branch; the warp-wide vote (needed only for the O
+        // rescale after the exponentials) stays off the path to the exponentials
+        const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
+        m_used = need ? m_new : m_used;
+        l *= alpha;
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
         // p = exp2(s * sl2 - m), packed to bf16 pairs; row sum in fp32 (four packed chains)
         if constexpr (C::kTurns) {
@@ -663,6 +661,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           pass_turn();
           ++taken;
         }
+        const bool any_need = __any_sync(0xffffffffu, need);
         if (!C::kSepP && any_need && nl > 0) {
           // the previous PV of this tile must be done before O_t is rescaled
           if (!warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 9))) return false;
