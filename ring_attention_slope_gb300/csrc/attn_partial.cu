@@ -576,11 +576,6 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         reg_fence(q1);
         reg_fence(q2);
         reg_fence(q3);
-        if (C::kSepP) {  // S_t is in registers: the next S MMA of this tile may overwrite it
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_sfree[t]);
-        }
         float sv[128];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -637,6 +632,11 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           pk[i] = (i & 15) < kPolyPairsPer16
                       ? softmax_pair_poly(sv[2 * i], sv[2 * i + 1], sl2v, negm, acc[i & 3], poly)
                       : softmax_pair(sv[2 * i], sv[2 * i + 1], sl2v, negm, acc[i & 3]);
+          if (C::kSepP && i == 15) {  // S_t is in registers: the next S MMA of this tile may overwrite it
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_sfree[t]);
+          }
           if ((i & 15) == 15) {
             const int c = i >> 4;  // chunk c of P is complete
             if constexpr (!C::kSepP) {
