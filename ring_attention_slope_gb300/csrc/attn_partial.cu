@@ -595,18 +595,28 @@ __global__ void __launch_bounds__(kK1Threads, 1)
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
             if (static_cast<uint32_t>(c - lo) > span) sv[c] = -INFINITY;
-          // row max over the visible scores: four independent chains of 3-input max
-          float a0 = sv[0], a1 = sv[1], a2 = sv[2], a3 = sv[3];
+          // row max over the visible scores, per 32-column quarter: a quarter wholly visible
+          // to this lane keeps the load's maximum, a hidden one gives -inf; only a quarter
+          // that some lane of the warp sees in part takes a max over the masked scores
+          float qm[4] = {q0, q1, q2, q3};
 #pragma unroll
-          for (int i = 4; i < 124; i += 8) {
-            a0 = fmax3(a0, sv[i], sv[i + 1]);
-            a1 = fmax3(a1, sv[i + 2], sv[i + 3]);
-            a2 = fmax3(a2, sv[i + 4], sv[i + 5]);
-            a3 = fmax3(a3, sv[i + 6], sv[i + 7]);
+          for (int j = 0; j < 4; ++j) {
+            const bool all_vis = lo <= 32 * j && 32 * j + 31 <= hi;
+            const bool none_vis = hi < 32 * j || lo > 32 * j + 31;
+            if (__any_sync(0xffffffffu, !all_vis && !none_vis)) {
+              float a = fmax3(sv[32 * j], sv[32 * j + 1], sv[32 * j + 2]);
+              float b = fmax3(sv[32 * j + 3], sv[32 * j + 4], sv[32 * j + 5]);
+#pragma unroll
+              for (int i = 6; i < 30; i += 4) {
+                a = fmax3(a, sv[32 * j + i], sv[32 * j + i + 1]);
+                b = fmax3(b, sv[32 * j + i + 2], sv[32 * j + i + 3]);
+              }
+              qm[j] = fmax3(a, b, fmaxf(sv[32 * j + 30], sv[32 * j + 31]));
+            } else {
+              qm[j] = all_vis ? qm[j] : -INFINITY;
+            }
           }
-          a0 = fmax3(a0, sv[124], sv[125]);
-          a1 = fmax3(a1, sv[126], sv[127]);
-          mx = fmax3(a0, a1, fmaxf(a2, a3));
+          mx = fmax3(qm[0], qm[1], fmaxf(qm[2], qm[3]));
         }
         const float m_new = mx * sl2;
         const bool need = m_new > m_used + kRescaleThreshold;
