@@ -209,8 +209,9 @@ SLOPE_API size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t 
  *   q, k, v, out, lse: caller-owned device buffers, dense; the other
  *     arguments are those of slope_cp_prefill.
  *
- * Nothing is allocated.  The call returns once the work is queued; the host
- * outputs are valid when copy_out_stream reaches that point.  Two calls with
+ * Nothing is allocated.  The call returns once the work is queued: the host
+ * inputs must stay valid and unchanged until copy_in_stream has passed this
+ * call, and the host outputs are valid once copy_out_stream has.  Two calls with
  * different device buffers overlap: the second call's input copies run while
  * the first computes, and the first call's output copies while the second
  * computes (the workspace is shared safely: both computes run on

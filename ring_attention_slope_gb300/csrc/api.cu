@@ -568,15 +568,19 @@ BufferSetEvents* buffer_set(int device, const void* key) {
   int cur = 0;
   if (cudaGetDevice(&cur) != cudaSuccess) return nullptr;
   if (b.in_ready != nullptr) {
-    if (b.device != cur && cudaSetDevice(b.device) != cudaSuccess) return nullptr;
-    if (b.used) cudaEventSynchronize(b.drained);
-    if (b.device != device) {
+    // the slot's events belong to b.device: work on them with that device current, and
+    // make `cur` current again on every path
+    const bool switched = b.device != cur;
+    if (switched && cudaSetDevice(b.device) != cudaSuccess) return nullptr;
+    const cudaError_t sync = b.used ? cudaEventSynchronize(b.drained) : cudaSuccess;
+    if (sync == cudaSuccess && b.device != device) {
       cudaEventDestroy(b.in_ready);
       cudaEventDestroy(b.consumed);
       cudaEventDestroy(b.drained);
       b.in_ready = b.consumed = b.drained = nullptr;
     }
-    if (b.device != cur && cudaSetDevice(cur) != cudaSuccess) return nullptr;
+    if (switched && cudaSetDevice(cur) != cudaSuccess) return nullptr;
+    if (sync != cudaSuccess) return nullptr;
   }
   b.used = false;
   b.key = key;
