@@ -13,7 +13,8 @@ metric through ``slope_cp_prefill_host`` with pinned host buffers: every step
 copies Q/K/V in and out/lse back inside the timed region, two device-buffer
 sets letting each step's copies overlap its neighbours' compute.
 ``fused_single_launch`` is the same attention as one launch over the whole
-sequence (no partials, no merge).  ``--impl reference`` times the fp64 CPU
+sequence (no partials, no merge); ``bf16_partials`` is the step with the
+partial outputs kept in bf16 (``slope_cp_prefill_ex``).  ``--impl reference`` times the fp64 CPU
 oracle on a bounded sample of the same workload (rank 0 only).
 """
 from __future__ import annotations
@@ -315,6 +316,10 @@ def run_gpu(args, w):
     # ---- the same attention as one launch (bf16 out, no partials, no merge): the fused single-GPU form
     fused = run_fused(slope, torch, w, window, q, k, v, stream, args, barrier, dist)
 
+    # ---- the same step with the partials kept in bf16 between the attention launches and the merge
+    bf16p = run_bf16_partials(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream, args, barrier, dist)
+    bf16p["gpu_launches_per_step"] = counts[0]  # the same launches as the fp32-partial step
+
     # ---- end to end through the public call with pinned host buffers
     e2e = None if args.no_e2e else run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier,
                                            dist)
@@ -344,6 +349,7 @@ def run_gpu(args, w):
                            "avg_launch_ms": k2_ms / max(1, k2_n)},
         "e2e": e2e,
         "fused_single_launch": fused,
+        "bf16_partials": bf16p,
         "gpu_launches": int(sum(counts)),
         "clocks": clocks,
     }
@@ -410,6 +416,33 @@ def run_fused(slope, torch, w, window, q, k, v, stream, args, barrier, dist):
     return {"value": job_tflops(workload_flops(w, window), args.steps, world, ms), "unit": UNIT,
             "ms_per_step": ms / args.steps, "api": "slope_attn_partial over the whole sequence, bf16 out",
             "gpu_launches_per_step": 1}
+
+
+def run_bf16_partials(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream, args, barrier, dist):
+    """The benchmark step with SLOPE_CP_BF16_PARTIALS: the same launches, the partial outputs written and
+    merged as bf16 (half the workspace, half the merge's partial reads)."""
+    nbytes = slope.cp_prefill_workspace_size(w.S, w.Hq, w.dv, n, w.layout, sizes, bf16_partials=True)
+    ws16 = torch.empty((nbytes,), dtype=torch.uint8, device="cuda")
+
+    def step():
+        slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window, out=out, lse=lse, workspace=ws16,
+                         bf16_partials=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), dist, "cuda")
+    world = dist.get_world_size() if dist is not None else 1
+    return {"value": job_tflops(workload_flops(w, window), args.steps, world, ms), "unit": UNIT,
+            "ms_per_step": ms / args.steps, "api": "slope_cp_prefill_ex(SLOPE_CP_BF16_PARTIALS)",
+            "workspace_bytes": nbytes}
 
 
 def run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier, dist):

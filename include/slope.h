@@ -119,9 +119,12 @@ SLOPE_API slope_status slope_attn_partial(const slope_tensor* q, const slope_ten
  *   L   = log sum_k exp(lse_k)            (max-shifted; all -inf gives -inf)
  *   out = sum_k exp(lse_k - L) * out_k     (partials with lse_k = -inf are skipped)
  *
- *   outs[k] fp32 [S, H, dv], lses[k] fp32 rank 2 [H, S] (any strides), 1 <= n <= 32.
+ *   outs[k] fp32 or bf16 [S, H, dv], all of one dtype (else SLOPE_ERR_DTYPE);
+ *        lses[k] fp32 rank 2 [H, S] (any strides), 1 <= n <= 32.  bf16 partials
+ *        are widened to fp32 as they are read; the sums run in fp32 either way.
  *   out: bf16 or fp32 [S, H, dv] (innermost stride 1, row/head strides multiples
- *        of 4 elements, 16-byte aligned pointers for out and every outs[k]).
+ *        of 4 elements; pointers 16-byte aligned for fp32, 8-byte for bf16, for
+ *        out and every outs[k]).
  *   lse: fp32 [H, S], or NULL to skip writing it.
  * `outs` and `lses` are host arrays of n descriptors.
  */
@@ -192,6 +195,36 @@ SLOPE_API slope_status slope_cp_prefill_static_scratch(const slope_tensor* q, co
 /* Workspace bytes slope_cp_prefill needs for these sizes (0 on invalid arguments). */
 SLOPE_API size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t dv, int n_chunks, slope_layout layout,
                                        const int64_t* chunk_sizes);
+
+/* Flags of slope_cp_prefill_ex. */
+#define SLOPE_CP_BF16_PARTIALS 1u /* keep the partial outputs in bf16 (lse stays fp32) */
+
+/*
+ * slope_cp_prefill with options.  flags = 0 is slope_cp_prefill exactly.
+ *
+ * SLOPE_CP_BF16_PARTIALS: each partial output travels from the attention
+ * launches to the merge rounded to bf16 (round to nearest even) instead of
+ * fp32: half the workspace and half the bytes the merge reads.  The partial
+ * log-sum-exps stay fp32 and the merge sums in fp32.  The pages name Ring
+ * Attention (Moreh, section "Introduction to Context Parallelism") without
+ * fixing the precision in which a step's partial result is kept; the merge is
+ * the exact one of slope_lse_merge either way.  Since the merge weights are
+ * positive and sum to 1, rounding each partial once more moves the final
+ * output by at most one bf16 rounding (relative 2^-8) of the largest partial
+ * element, before the output's own rounding when out is bf16.
+ *
+ * Unknown flag bits return SLOPE_ERR_UNSUPPORTED.  The workspace must hold
+ * slope_cp_prefill_workspace_size_ex(..., flags) bytes (the flags = 0 size is
+ * always enough).
+ */
+SLOPE_API slope_status slope_cp_prefill_ex(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v,
+                                           int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
+                                           int64_t window, float scale, unsigned flags, slope_tensor* out,
+                                           slope_tensor* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes slope_cp_prefill_ex needs for these sizes and flags (0 on invalid arguments). */
+SLOPE_API size_t slope_cp_prefill_workspace_size_ex(int64_t S, int64_t Hq, int64_t dv, int n_chunks,
+                                                    slope_layout layout, const int64_t* chunk_sizes, unsigned flags);
 
 /*
  * slope_cp_prefill on inputs and outputs in host memory: the same attention

@@ -56,7 +56,11 @@ _lib = None
 EXPORTED = ["slope_attn_partial", "slope_lse_merge", "slope_cp_prefill", "slope_cp_prefill_workspace_size",
             "slope_cp_prefill_timed", "slope_cp_prefill_plan", "slope_device_status",
             "slope_debug_timeout_selftest", "slope_status_string", "slope_version", "slope_last_error",
-            "slope_cp_prefill_static_scratch", "slope_cp_prefill_host"]
+            "slope_cp_prefill_static_scratch", "slope_cp_prefill_host", "slope_cp_prefill_ex",
+            "slope_cp_prefill_workspace_size_ex"]
+
+# flags of slope_cp_prefill_ex (include/slope.h)
+CP_BF16_PARTIALS = 1
 
 
 def build(force: bool = False) -> str:
@@ -105,6 +109,11 @@ def load():
     lib.slope_cp_prefill_host.argtypes = [T, T, T, T, T, T, T, T, T, T, c_int, c_int, P(i64), c_int, i64, f32, vp,
                                           ctypes.c_size_t, vp, vp, vp]
     lib.slope_cp_prefill_host.restype = c_int
+    lib.slope_cp_prefill_ex.argtypes = [T, T, T, c_int, c_int, P(i64), c_int, i64, f32, ctypes.c_uint, T, T, vp,
+                                        ctypes.c_size_t, vp]
+    lib.slope_cp_prefill_ex.restype = c_int
+    lib.slope_cp_prefill_workspace_size_ex.argtypes = [i64, i64, i64, c_int, c_int, P(i64), ctypes.c_uint]
+    lib.slope_cp_prefill_workspace_size_ex.restype = ctypes.c_size_t
     _lib = lib
     return lib
 
@@ -199,7 +208,7 @@ def attn_partial(q, k, v, *, q_off=0, kv_off=0, causal=True, window=0, scale=0.0
 
 
 def lse_merge(outs, lses, *, out=None, lse=None, out_dtype=None, stream=None):
-    """Exact log-sum-exp merge of partials outs[k] fp32 [S,H,dv], lses[k] fp32 [H,S]."""
+    """Exact log-sum-exp merge of partials outs[k] fp32 or bf16 [S,H,dv] (one dtype), lses[k] fp32 [H,S]."""
     torch = _torch()
     n = len(outs)
     if n != len(lses) or n == 0:
@@ -217,12 +226,15 @@ def lse_merge(outs, lses, *, out=None, lse=None, out_dtype=None, stream=None):
     return out, lse
 
 
-def cp_prefill_workspace_size(S, Hq, dv, n_chunks, layout, chunk_sizes=None) -> int:
+def cp_prefill_workspace_size(S, Hq, dv, n_chunks, layout, chunk_sizes=None, bf16_partials=False) -> int:
     arr, ptr = _chunk_array(chunk_sizes)
+    if bf16_partials:
+        return int(load().slope_cp_prefill_workspace_size_ex(int(S), int(Hq), int(dv), int(n_chunks), _layout(layout),
+                                                             ptr, CP_BF16_PARTIALS))
     return int(load().slope_cp_prefill_workspace_size(int(S), int(Hq), int(dv), int(n_chunks), _layout(layout), ptr))
 
 
-def _prep_cp(q, v, n_chunks, layout, chunk_sizes, out, lse, workspace, out_dtype, want_lse):
+def _prep_cp(q, v, n_chunks, layout, chunk_sizes, out, lse, workspace, out_dtype, want_lse, bf16_partials=False):
     torch = _torch()
     S, Hq, _ = q.shape
     dv = v.shape[2]
@@ -231,7 +243,7 @@ def _prep_cp(q, v, n_chunks, layout, chunk_sizes, out, lse, workspace, out_dtype
     if lse is None and want_lse:
         lse = torch.empty((Hq, S), dtype=torch.float32, device=q.device)
     if workspace is None:
-        nbytes = cp_prefill_workspace_size(S, Hq, dv, n_chunks, layout, chunk_sizes)
+        nbytes = cp_prefill_workspace_size(S, Hq, dv, n_chunks, layout, chunk_sizes, bf16_partials)
         if nbytes == 0:
             raise SlopeError(-5, "slope_cp_prefill_workspace_size")
         workspace = torch.empty((nbytes,), dtype=torch.uint8, device=q.device)
@@ -239,20 +251,28 @@ def _prep_cp(q, v, n_chunks, layout, chunk_sizes, out, lse, workspace, out_dtype
 
 
 def cp_prefill(q, k, v, n_chunks, layout="zigzag", *, chunk_sizes=None, causal=True, window=0, scale=0.0,
-               out=None, lse=None, workspace=None, out_dtype=None, want_lse=True, stream=None):
+               out=None, lse=None, workspace=None, out_dtype=None, want_lse=True, stream=None, bf16_partials=False):
     """Context-parallel prefill attention of one layer (ring steps or chunks run in order, then merged).
 
     Returns ``(out, lse)``: out bf16 (default) or fp32 [S,Hq,dv], lse fp32 [Hq,S] (None if not wanted).
+    ``bf16_partials`` keeps the partial outputs in bf16 between the attention launches and the merge
+    (slope_cp_prefill_ex with SLOPE_CP_BF16_PARTIALS); otherwise slope_cp_prefill runs.
     """
-    out, lse, workspace = _prep_cp(q, v, n_chunks, layout, chunk_sizes, out, lse, workspace, out_dtype, want_lse)
+    out, lse, workspace = _prep_cp(q, v, n_chunks, layout, chunk_sizes, out, lse, workspace, out_dtype, want_lse,
+                                   bf16_partials)
     arr, ptr = _chunk_array(chunk_sizes)
     dq, dk, dvv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     dl = _desc(lse) if lse is not None else None
-    st = load().slope_cp_prefill(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dvv), int(n_chunks),
-                                 _layout(layout), ptr, int(bool(causal)), int(window), float(scale),
-                                 ctypes.byref(do), ctypes.byref(dl) if dl is not None else None,
-                                 ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
-    _check(st, "slope_cp_prefill")
+    args_head = (ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dvv), int(n_chunks), _layout(layout), ptr,
+                 int(bool(causal)), int(window), float(scale))
+    args_tail = (ctypes.byref(do), ctypes.byref(dl) if dl is not None else None,
+                 ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    if bf16_partials:
+        st = load().slope_cp_prefill_ex(*args_head, CP_BF16_PARTIALS, *args_tail)
+        _check(st, "slope_cp_prefill_ex")
+    else:
+        st = load().slope_cp_prefill(*args_head, *args_tail)
+        _check(st, "slope_cp_prefill")
     return out, lse
 
 

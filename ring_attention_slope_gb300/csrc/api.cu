@@ -343,9 +343,11 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct WorkspaceLayout {
   size_t out_bytes, lse_offset, total;
 };
-WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t dv, int n_planes) {
+// Partial planes (fp32, or bf16 under SLOPE_CP_BF16_PARTIALS), then the fp32 lse planes.
+WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t dv, int n_planes, unsigned flags) {
   WorkspaceLayout w;
-  w.out_bytes = static_cast<size_t>(S) * Hq * dv * sizeof(float);
+  const size_t elem = (flags & SLOPE_CP_BF16_PARTIALS) ? 2 : sizeof(float);
+  w.out_bytes = static_cast<size_t>(S) * Hq * dv * elem;
   w.lse_offset = round_up(w.out_bytes * n_planes, 256);
   w.total = w.lse_offset + round_up(static_cast<size_t>(S) * Hq * sizeof(float) * n_planes, 256);
   return w;
@@ -354,9 +356,10 @@ WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t dv, int n_planes
 // Every argument check of cp_prefill_impl, with no side effect; fills `plan`.
 slope_status cp_prefill_check(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
                               slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
-                              const slope_tensor* out, const slope_tensor* lse, const void* workspace,
-                              size_t workspace_bytes, Plan& plan) {
+                              unsigned flags, const slope_tensor* out, const slope_tensor* lse,
+                              const void* workspace, size_t workspace_bytes, Plan& plan) {
   slope_status st;
+  if (flags & ~static_cast<unsigned>(SLOPE_CP_BF16_PARTIALS)) return SLOPE_ERR_UNSUPPORTED;
   if ((st = check_qkv(q)) != SLOPE_OK || (st = check_qkv(k)) != SLOPE_OK || (st = check_qkv(v)) != SLOPE_OK)
     return st;
   const int64_t S = q->shape[0], Hq = q->shape[1], dqk = q->shape[2];
@@ -370,30 +373,31 @@ slope_status cp_prefill_check(const slope_tensor* q, const slope_tensor* k, cons
   if (S == 0) return SLOPE_ERR_SHAPE;
   if ((st = build_plan(S, n_chunks, layout, chunk_sizes, causal, window, plan)) != SLOPE_OK) return st;
   if (plan.n_planes > kMaxMerge) return SLOPE_ERR_UNSUPPORTED;
-  const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes);
+  const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes, flags);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < wl.total) return SLOPE_ERR_WORKSPACE;
   return SLOPE_OK;
 }
 
 slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
                              slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
-                             float scale, slope_tensor* out, slope_tensor* lse, void* workspace,
+                             float scale, unsigned flags, slope_tensor* out, slope_tensor* lse, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream, Timing* tm) {
   slope_status st;
   Plan plan;
-  if ((st = cp_prefill_check(q, k, v, n_chunks, layout, chunk_sizes, causal, window, out, lse, workspace,
+  if ((st = cp_prefill_check(q, k, v, n_chunks, layout, chunk_sizes, causal, window, flags, out, lse, workspace,
                              workspace_bytes, plan)) != SLOPE_OK)
     return st;
   const int64_t S = q->shape[0], Hq = q->shape[1], dqk = q->shape[2];
   const int64_t Hkv = k->shape[1], dv = v->shape[2];
-  const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes);
+  const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes, flags);
+  const bool bf16_partials = (flags & SLOPE_CP_BF16_PARTIALS) != 0;
   int* status = device_status_ptr();
   if (status == nullptr) return cuda_fail("device status word (cudaGetSymbolAddress)");
 
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, q) || !make_map(&tk, k) || !make_map(&tv, v)) return cuda_fail("cuTensorMapEncodeTiled");
 
-  float* planes = static_cast<float*>(workspace);
+  void* planes = workspace;  // fp32 or bf16 elements
   float* lse_planes = reinterpret_cast<float*>(static_cast<char*>(workspace) + wl.lse_offset);
   AttnParams base{};
   base.Hq = static_cast<int32_t>(Hq);
@@ -404,7 +408,7 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   base.kv_pos_off = 0;
   base.write_empty_out = 0;  // the merge never reads partials whose lse is -inf
   base.scale_log2 = resolve_scale(scale, dqk) * 1.44269504088896340736f;
-  base.out = planes;
+  base.out = static_cast<float*>(planes);  // the kernel reinterprets it as bf16 under out_bf16
   base.out_srow = Hq * dv;
   base.out_shead = dv;
   base.out_splane = S * Hq * dv;
@@ -416,9 +420,9 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   base.wait_limit_ns = wait_limit_ns();
   CUtensorMap to;
   base.out_plane_rows = S;
-  base.out_bf16 = 0;
+  base.out_bf16 = bf16_partials ? 1 : 0;
   base.out_tma =
-      make_out_map(&to, planes, false, static_cast<int64_t>(plan.n_planes) * S, Hq, dv, Hq * dv, dv) ? 1 : 0;
+      make_out_map(&to, planes, bf16_partials, static_cast<int64_t>(plan.n_planes) * S, Hq, dv, Hq * dv, dv) ? 1 : 0;
   if (!base.out_tma) to = tq;  // never used
 
   // A plane none of whose items sees a key (ring steps that a sliding window leaves
@@ -460,10 +464,11 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   mp.H = static_cast<int32_t>(Hq);
   mp.dv = static_cast<int32_t>(dv);
   mp.S = S;
+  mp.in_bf16 = bf16_partials ? 1 : 0;
   for (int pl = 0; pl < plan.n_planes; ++pl) {
     if (!plane_live[static_cast<size_t>(pl)]) continue;
     const int m = mp.n++;
-    mp.outs[m] = planes + static_cast<int64_t>(pl) * S * Hq * dv;
+    mp.outs[m] = static_cast<const char*>(planes) + static_cast<size_t>(pl) * wl.out_bytes;
     mp.lses[m] = lse_planes + static_cast<int64_t>(pl) * S * Hq;
     mp.o_srow[m] = Hq * dv;
     mp.o_shead[m] = dv;
@@ -691,9 +696,10 @@ slope_status slope_lse_merge(const slope_tensor* outs, const slope_tensor* lses,
   if (lse != nullptr && (st = check_lse(lse, H, S)) != SLOPE_OK) return st;
   MergeParams mp{};
   for (int i = 0; i < n; ++i) {
-    if ((st = check_out(&outs[i], S, H, dv, false)) != SLOPE_OK) return st;
+    if ((st = check_out(&outs[i], S, H, dv, true)) != SLOPE_OK) return st;
+    if (outs[i].dtype != outs[0].dtype) return SLOPE_ERR_DTYPE;  // one dtype for all partials
     if ((st = check_lse(&lses[i], H, S)) != SLOPE_OK) return st;
-    mp.outs[i] = static_cast<const float*>(outs[i].data);
+    mp.outs[i] = outs[i].data;
     mp.o_srow[i] = outs[i].stride[0];
     mp.o_shead[i] = outs[i].stride[1];
     mp.lses[i] = static_cast<const float*>(lses[i].data);
@@ -705,6 +711,7 @@ slope_status slope_lse_merge(const slope_tensor* outs, const slope_tensor* lses,
   mp.H = static_cast<int32_t>(H);
   mp.dv = static_cast<int32_t>(dv);
   mp.S = S;
+  mp.in_bf16 = outs[0].dtype == SLOPE_BF16 ? 1 : 0;
   mp.out = out->data;
   mp.out_bf16 = out->dtype == SLOPE_BF16 ? 1 : 0;
   mp.out_srow = out->stride[0];
@@ -716,19 +723,33 @@ slope_status slope_lse_merge(const slope_tensor* outs, const slope_tensor* lses,
   return e == cudaSuccess ? SLOPE_OK : cuda_fail("merge kernel launch", e);
 }
 
-size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t dv, int n_chunks, slope_layout layout,
-                                       const int64_t* chunk_sizes) {
+size_t slope_cp_prefill_workspace_size_ex(int64_t S, int64_t Hq, int64_t dv, int n_chunks, slope_layout layout,
+                                          const int64_t* chunk_sizes, unsigned flags) {
   if (S <= 0 || S > kMaxSeq || Hq <= 0 || (dv != 64 && dv != 128)) return 0;
+  if (flags & ~static_cast<unsigned>(SLOPE_CP_BF16_PARTIALS)) return 0;
   Plan plan;
   if (build_plan(S, n_chunks, layout, chunk_sizes, 1, 0, plan) != SLOPE_OK) return 0;
-  return workspace_layout(S, Hq, dv, plan.n_planes).total;
+  return workspace_layout(S, Hq, dv, plan.n_planes, flags).total;
+}
+
+size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t dv, int n_chunks, slope_layout layout,
+                                       const int64_t* chunk_sizes) {
+  return slope_cp_prefill_workspace_size_ex(S, Hq, dv, n_chunks, layout, chunk_sizes, 0u);
 }
 
 slope_status slope_cp_prefill(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
                               slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
                               float scale, slope_tensor* out, slope_tensor* lse, void* workspace,
                               size_t workspace_bytes, void* stream) {
-  return cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, out, lse, workspace,
+  return cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, 0u, out, lse, workspace,
+                         workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+slope_status slope_cp_prefill_ex(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
+                                 slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
+                                 float scale, unsigned flags, slope_tensor* out, slope_tensor* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  return cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, flags, out, lse, workspace,
                          workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
 }
 
@@ -776,7 +797,7 @@ slope_status slope_cp_prefill_timed(const slope_tensor* q, const slope_tensor* k
       if (needed > n_event_pairs) return SLOPE_ERR_SHAPE;
     }
   }
-  slope_status st = cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, out, lse,
+  slope_status st = cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, 0u, out, lse,
                                     workspace, workspace_bytes, static_cast<cudaStream_t>(stream), &tm);
   *n_launches = tm.count;
   return st;
@@ -802,7 +823,7 @@ slope_status slope_cp_prefill_host(const slope_tensor* q_host, const slope_tenso
   }
   // every check of the compute runs before anything is queued
   Plan probe;
-  slope_status st = cp_prefill_check(q, k, v, n_chunks, layout, chunk_sizes, causal, window, out, lse, workspace,
+  slope_status st = cp_prefill_check(q, k, v, n_chunks, layout, chunk_sizes, causal, window, 0u, out, lse, workspace,
                                      workspace_bytes, probe);
   if (st != SLOPE_OK) return st;
   if (out->dtype != SLOPE_BF16 && out->dtype != SLOPE_F32) return SLOPE_ERR_DTYPE;
@@ -827,7 +848,7 @@ slope_status slope_cp_prefill_host(const slope_tensor* q_host, const slope_tenso
   if ((e = cudaStreamWaitEvent(s_c, b->in_ready, 0)) != cudaSuccess) return cuda_fail("cudaStreamWaitEvent", e);
   if (b->used && (e = cudaStreamWaitEvent(s_c, b->drained, 0)) != cudaSuccess)
     return cuda_fail("cudaStreamWaitEvent", e);
-  st = cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, out, lse, workspace,
+  st = cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, 0u, out, lse, workspace,
                        workspace_bytes, s_c, nullptr);
   if (st != SLOPE_OK) return st;
   if ((e = cudaEventRecord(b->consumed, s_c)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);

@@ -69,7 +69,8 @@ struct MergeParams {
   int32_t dv;
   int32_t out_bf16;
   int64_t S;
-  const float* outs[kMaxMerge];
+  int32_t in_bf16;  // partials are bf16 (else fp32)
+  const void* outs[kMaxMerge];
   const float* lses[kMaxMerge];
   int64_t o_srow[kMaxMerge], o_shead[kMaxMerge];
   int64_t l_srow[kMaxMerge], l_shead[kMaxMerge];

@@ -27,7 +27,9 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // resident to hide the two dependent loads (lse, then partials): at n <= 8 four blocks
 // of 256 threads per SM.  Measured on one GB300 against the old fixed bound of 32:
 // 2 partials 2.6 -> 6.8 TB/s, 8 partials 5.3 -> 6.7 TB/s, 16 partials 6.4 -> 7.0 TB/s.
-template <int DV, bool OUT_BF16, int NMAX>
+// IN_BF16: the partials are bf16 (each thread then reads 4 columns = 8 bytes per float4
+// position), halving the bytes read; accumulation stays fp32.
+template <int DV, bool OUT_BF16, int NMAX, bool IN_BF16>
 __global__ void __launch_bounds__(kMergeThreads, NMAX <= 8 ? 4 : 2)
     lse_merge_kernel(const __grid_constant__ MergeParams p) {
   // DV/16 threads per (row, head), four float4 columns each: thread q owns float4
@@ -74,11 +76,23 @@ __global__ void __launch_bounds__(kMergeThreads, NMAX <= 8 ? 4 : 2)
         const int k = b + i;
         const bool live = k < p.n && lk[k] != -INFINITY;
         w[i] = live ? ex2_approx((lk[k] - L) * kLog2e) : 0.f;
-        const float4* src = live ? reinterpret_cast<const float4*>(p.outs[k] + row * p.o_srow[k] + h * p.o_shead[k])
-                                 : nullptr;
+        const int64_t eoff = row * p.o_srow[k] + h * p.o_shead[k];
+        if constexpr (IN_BF16) {
+          const uint2* src = live ? reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.outs[k]) + eoff)
+                                  : nullptr;
 #pragma unroll
-        for (int j = 0; j < kVec; ++j)
-          v[i][j] = live ? __ldcs(src + q + kTpp * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j = 0; j < kVec; ++j) {
+            const uint2 r = live ? __ldcs(src + q + kTpp * j) : make_uint2(0u, 0u);
+            v[i][j] = make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xffff0000u),
+                                  __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xffff0000u));
+          }
+        } else {
+          const float4* src = live ? reinterpret_cast<const float4*>(static_cast<const float*>(p.outs[k]) + eoff)
+                                   : nullptr;
+#pragma unroll
+          for (int j = 0; j < kVec; ++j)
+            v[i][j] = live ? __ldcs(src + q + kTpp * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
 #pragma unroll
       for (int i = 0; i < kBatch; ++i)
@@ -107,24 +121,29 @@ __global__ void __launch_bounds__(kMergeThreads, NMAX <= 8 ? 4 : 2)
   if (q == 0 && p.lse != nullptr) p.lse[row * p.lse_srow + h * p.lse_shead] = L;
 }
 
-template <int DV, bool BF16, int NMAX>
+template <int DV, bool BF16, int NMAX, bool IN_BF16>
 cudaError_t launch_n(const MergeParams& p, cudaStream_t stream) {
   const int64_t threads = p.S * p.H * (DV / 16);
   if (threads == 0) return cudaSuccess;
   const int64_t blocks = (threads + kMergeThreads - 1) / kMergeThreads;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  lse_merge_kernel<DV, BF16, NMAX><<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(p);
+  lse_merge_kernel<DV, BF16, NMAX, IN_BF16><<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int DV, bool BF16, bool IN_BF16>
+cudaError_t launch_in(const MergeParams& p, cudaStream_t stream) {
+  static_assert(kMaxMerge == 32, "plane-count bounds below");
+  if (p.n <= 2) return launch_n<DV, BF16, 2, IN_BF16>(p, stream);
+  if (p.n <= 4) return launch_n<DV, BF16, 4, IN_BF16>(p, stream);
+  if (p.n <= 8) return launch_n<DV, BF16, 8, IN_BF16>(p, stream);
+  if (p.n <= 16) return launch_n<DV, BF16, 16, IN_BF16>(p, stream);
+  return launch_n<DV, BF16, 32, IN_BF16>(p, stream);
 }
 
 template <int DV, bool BF16>
 cudaError_t launch_impl(const MergeParams& p, cudaStream_t stream) {
-  static_assert(kMaxMerge == 32, "plane-count bounds below");
-  if (p.n <= 2) return launch_n<DV, BF16, 2>(p, stream);
-  if (p.n <= 4) return launch_n<DV, BF16, 4>(p, stream);
-  if (p.n <= 8) return launch_n<DV, BF16, 8>(p, stream);
-  if (p.n <= 16) return launch_n<DV, BF16, 16>(p, stream);
-  return launch_n<DV, BF16, 32>(p, stream);
+  return p.in_bf16 ? launch_in<DV, BF16, true>(p, stream) : launch_in<DV, BF16, false>(p, stream);
 }
 
 }  // namespace

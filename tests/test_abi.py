@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_symbols()
-    assert len(names) == 13, names
+    assert len(names) == 15, names
     for n in names:
         assert hasattr(lib, n), f"{n} declared in slope.h but not exported"
     assert sorted(names) == sorted(slope.EXPORTED)
@@ -107,7 +107,37 @@ def test_attn_partial_and_merge_argument_errors(lib):
     l_bad = (slope.SlopeTensor * 2)(_t([Hq, Sq], dtype=1), _t([Hq, Sq + 1], dtype=1))
     assert lib.slope_lse_merge(o, l_bad, 2, ctypes.byref(fin), None, None) == E_SHAPE
     o_bad = (slope.SlopeTensor * 2)(_t([Sq, Hq, 64], dtype=1), _t([Sq, Hq, 64], dtype=0))
-    assert lib.slope_lse_merge(o_bad, l, 2, ctypes.byref(fin), None, None) == E_DTYPE
+    assert lib.slope_lse_merge(o_bad, l, 2, ctypes.byref(fin), None, None) == E_DTYPE  # mixed partial dtypes
+    o_bad = (slope.SlopeTensor * 2)(_t([Sq, Hq, 64], dtype=0), _t([Sq, Hq, 64], dtype=5))
+    assert lib.slope_lse_merge(o_bad, l, 2, ctypes.byref(fin), None, None) == E_DTYPE  # unknown dtype
+    o_bad = (slope.SlopeTensor * 2)(_t([Sq, Hq, 64], dtype=0), _t([Sq, Hq, 64], dtype=0, data=0x10004))
+    assert lib.slope_lse_merge(o_bad, l, 2, ctypes.byref(fin), None, None) == E_STRIDE  # bf16 partial: 8-B aligned
+
+
+def test_cp_prefill_ex_flags(lib):
+    """flags = 0 is slope_cp_prefill (same checks); unknown bits are refused before any launch;
+    bf16 partials need half the plane bytes."""
+    S, Hq, Hkv, d = 1024, 4, 1, 64
+    q, k, v = _t([S, Hq, d]), _t([S, Hkv, d]), _t([S, Hkv, d])
+    out, lse = _t([S, Hq, d]), _t([Hq, S], dtype=1)
+
+    def call(flags, ws_bytes=1 << 40, n=4):
+        return lib.slope_cp_prefill_ex(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), n, 1, None, 1, 0, 0.0,
+                                       flags, ctypes.byref(out), ctypes.byref(lse), 0x20000, ws_bytes, None)
+
+    assert call(2) == E_UNSUP
+    assert call(1 << 31) == E_UNSUP
+    assert call(1, n=5) == E_LAYOUT
+    lay = ctypes.c_int(1)
+    w0 = lib.slope_cp_prefill_workspace_size(S, Hq, d, 4, lay, None)
+    w1 = lib.slope_cp_prefill_workspace_size_ex(S, Hq, d, 4, lay, None, 1)
+    assert lib.slope_cp_prefill_workspace_size_ex(S, Hq, d, 4, lay, None, 0) == w0
+    assert lib.slope_cp_prefill_workspace_size_ex(S, Hq, d, 4, lay, None, 4) == 0
+    # planes: 4 x S x Hq x d x (4 | 2) bytes, then 4 fp32 lse planes (256-B rounded)
+    lse_bytes = 4 * S * Hq * 4
+    assert w0 == 4 * S * Hq * d * 4 + lse_bytes and w1 == 4 * S * Hq * d * 2 + lse_bytes
+    assert call(1, ws_bytes=w1 - 1) == E_WS
+    assert call(0, ws_bytes=w1) == E_WS  # fp32 partials need the larger workspace
 
 
 def test_workspace_size(lib):

@@ -262,11 +262,11 @@ def test_cp_prefill_mla_shape_small():
 
 # ---------------------------------------------------------------- full-size workloads, sampled rows/heads
 
-def check_full_workload(w, window, rows_random=4096):
+def check_full_workload(w, window, rows_random=4096, bf16_partials=False):
     q, k, v = wl.workload_qkv(w, device="cuda")
     sizes = wl.chunk_sizes(w)
     n = wl.n_chunks(w)
-    out, lse = slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window)
+    out, lse = slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window, bf16_partials=bf16_partials)
     torch.cuda.synchronize()
     assert slope.device_status() == (0, 0)
     rows = wl.sample_rows(w, n_random=rows_random)
@@ -275,7 +275,7 @@ def check_full_workload(w, window, rows_random=4096):
     ro, rl = oracle.attention(qc, kc, vc, causal=True, window=window, rows=rows, heads=heads)
     og = out[torch.from_numpy(rows).cuda()][:, heads].float().cpu()
     lg = lse[heads][:, torch.from_numpy(rows).cuda()].cpu()
-    compare(og, lg, ro, rl, f"{w.name} W={window}")
+    compare(og, lg, ro, rl, f"{w.name} W={window} bf16_partials={bf16_partials}")
     # properties at every row: finite outputs, lse >= the log of... finite and bounded
     assert torch.isfinite(out.float()).all()
     assert torch.isfinite(lse).all()
@@ -388,3 +388,79 @@ def test_cp_prefill_host_more_buffer_sets_than_tracked():
         torch.cuda.synchronize()
         assert torch.equal(outs[j], ro.cpu()), f"call {j} (buffer set {order[j]})"
     assert slope.device_status() == (0, 0)
+
+
+# ---------------------------------------------------------------- bf16 partials (slope_cp_prefill_ex)
+
+@pytest.mark.parametrize("dv", [64, 128])
+@pytest.mark.parametrize("n", [2, 5, 32])
+def test_lse_merge_bf16_partials_are_widened_exactly(dv, n):
+    """bf16 partials merge to exactly what their fp32 copies merge to (the merge widens each
+    element and then runs the fp32 arithmetic), and match the oracle on those partials."""
+    S, H = 333, 6
+    g = torch.Generator().manual_seed(7 * n + dv)
+    outs = [torch.randn(S, H, dv, generator=g).to(torch.bfloat16) for _ in range(n)]
+    lses = [torch.randn(H, S, generator=g) * 4 + 2 for _ in range(n)]
+    for i, l in enumerate(lses):
+        l[:, (torch.arange(S) % (i + 3)) == 1] = -math.inf
+    for l in lses:
+        l[:, :2] = -math.inf
+    lc = [x.cuda() for x in lses]
+    ob, lb = slope.lse_merge([o.cuda() for o in outs], lc, out_dtype=torch.float32)
+    of, lf = slope.lse_merge([o.float().cuda() for o in outs], lc, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(ob, of) and torch.equal(lb, lf)
+    ro, rl = oracle.merge([o.double().numpy() for o in outs], [x.double().numpy() for x in lses])
+    compare(ob.cpu(), lb.cpu(), ro, rl, f"bf16-partial merge n={n} dv={dv}")
+
+
+def _workspace_planes(ws, S, Hq, dv, n_planes, dtype):
+    """The partial planes [n_planes, S, Hq, dv] and fp32 lse planes [n_planes, S, Hq] (at the next
+    256-byte boundary) that a prefill leaves in its workspace."""
+    elem = 2 if dtype == torch.bfloat16 else 4
+    out_bytes = n_planes * S * Hq * dv * elem
+    lse_off = (out_bytes + 255) // 256 * 256
+    planes = ws[:out_bytes].view(dtype).view(n_planes, S, Hq, dv)
+    lses = ws[lse_off:lse_off + n_planes * S * Hq * 4].view(torch.float32).view(n_planes, S, Hq)
+    return planes, lses
+
+
+@pytest.mark.parametrize("layout,n,window,dqk,dv,sizes", [
+    ("zigzag", 4, 0, 64, 64, None), ("contiguous", 8, 0, 128, 128, None), ("zigzag", 8, 100, 64, 64, None),
+    ("chunked", 3, 0, 128, 64, [700, 1, 1347]), ("chunked", 2, 300, 192, 128, [1000, 1048])])
+def test_cp_prefill_bf16_partials_are_the_fp32_partials_rounded(layout, n, window, dqk, dv, sizes):
+    """SLOPE_CP_BF16_PARTIALS changes nothing but the rounding of each written partial element:
+    every written element is the fp32 path's element rounded to bf16 (round to nearest even),
+    the lse planes are bit-identical, and the result stays within the oracle tolerances and within
+    one bf16 rounding of the largest |v| of the fp32-partial result."""
+    S, Hq, Hkv = 2048, 4, 2
+    q, k, v = qkv(S, Hq, Hkv, dqk, dv, seed=53 + n + dqk)
+    n_planes = 2 if layout == "chunked" else n
+    ws32 = torch.full((slope.cp_prefill_workspace_size(S, Hq, dv, n, layout, sizes),), 0xFF, dtype=torch.uint8,
+                      device="cuda")
+    ws16 = torch.full((slope.cp_prefill_workspace_size(S, Hq, dv, n, layout, sizes, bf16_partials=True),), 0xFF,
+                      dtype=torch.uint8, device="cuda")
+    assert ws16.numel() < ws32.numel()
+    o32, l32 = slope.cp_prefill(q, k, v, n, layout, chunk_sizes=sizes, window=window, workspace=ws32,
+                                out_dtype=torch.float32)
+    o16, l16 = slope.cp_prefill(q, k, v, n, layout, chunk_sizes=sizes, window=window, workspace=ws16,
+                                out_dtype=torch.float32, bf16_partials=True)
+    torch.cuda.synchronize()
+    assert slope.device_status() == (0, 0)
+    p32, lp32 = _workspace_planes(ws32, S, Hq, dv, n_planes, torch.float32)
+    p16, lp16 = _workspace_planes(ws16, S, Hq, dv, n_planes, torch.bfloat16)
+    # same lse planes bit for bit, including the rows and planes neither run wrote
+    assert torch.equal(lp16.view(torch.int32), lp32.view(torch.int32))
+    written = torch.isfinite(lp32)  # rows of live planes that see a key (their out elements are written)
+    assert written.any()
+    assert torch.equal(p16[written].view(torch.int16), p32[written].to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(l16, l32)
+    # a partial element is a convex combination of v (up to the bf16 rounding of P): |x| <= 1.01 max|v|
+    bound = 2.0 ** -8 * 1.01 * v.float().abs().max().item() + 1e-5
+    assert (o16 - o32).abs().max().item() <= bound
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, window=window)
+    compare(o16.cpu(), l16.cpu(), ro, rl, f"bf16 partials {layout} n={n} W={window}")
+
+
+def test_full_causal_gqa_s32k_zigzag8_bf16_partials():
+    check_full_workload(wl.WORKLOADS[1], 0, rows_random=2048, bf16_partials=True)
