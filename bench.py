@@ -14,7 +14,8 @@ copies Q/K/V in and out/lse back inside the timed region, two device-buffer
 sets letting each step's copies overlap its neighbours' compute.
 ``fused_single_launch`` is the same attention as one launch over the whole
 sequence (no partials, no merge); ``bf16_partials`` is the step with the
-partial outputs kept in bf16 (``slope_cp_prefill_ex``).  ``--impl reference`` times the fp64 CPU
+partial outputs kept in bf16 (``slope_cp_prefill_ex``); ``ulysses`` is the
+head-sharded layout (one KV head group per rank, no merge).  ``--impl reference`` times the fp64 CPU
 oracle on a bounded sample of the same workload (rank 0 only).
 """
 from __future__ import annotations
@@ -320,6 +321,9 @@ def run_gpu(args, w):
     bf16p = run_bf16_partials(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream, args, barrier, dist)
     bf16p["gpu_launches_per_step"] = counts[0]  # the same launches as the fp32-partial step
 
+    # ---- the same attention in the head-sharded (Ulysses) layout
+    ulysses = run_ulysses(slope, torch, w, window, q, k, v, out, lse, stream, args, barrier, dist)
+
     # ---- end to end through the public call with pinned host buffers
     e2e = None if args.no_e2e else run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier,
                                            dist)
@@ -350,6 +354,7 @@ def run_gpu(args, w):
         "e2e": e2e,
         "fused_single_launch": fused,
         "bf16_partials": bf16p,
+        "ulysses": ulysses,
         "gpu_launches": int(sum(counts)),
         "clocks": clocks,
     }
@@ -418,16 +423,8 @@ def run_fused(slope, torch, w, window, q, k, v, stream, args, barrier, dist):
             "gpu_launches_per_step": 1}
 
 
-def run_bf16_partials(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream, args, barrier, dist):
-    """The benchmark step with SLOPE_CP_BF16_PARTIALS: the same launches, the partial outputs written and
-    merged as bf16 (half the workspace, half the merge's partial reads)."""
-    nbytes = slope.cp_prefill_workspace_size(w.S, w.Hq, w.dv, n, w.layout, sizes, bf16_partials=True)
-    ws16 = torch.empty((nbytes,), dtype=torch.uint8, device="cuda")
-
-    def step():
-        slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window, out=out, lse=lse, workspace=ws16,
-                         bf16_partials=True)
-
+def time_variant(torch, step, stream, args, barrier, dist):
+    """(ms per step, world size) of `step` run args.steps times after its warm-up, device-timed on `stream`."""
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -439,10 +436,41 @@ def run_bf16_partials(slope, torch, w, n, sizes, window, q, k, v, out, lse, stre
     b.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b), dist, "cuda")
-    world = dist.get_world_size() if dist is not None else 1
+    return ms, dist.get_world_size() if dist is not None else 1
+
+
+def run_bf16_partials(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream, args, barrier, dist):
+    """The benchmark step with SLOPE_CP_BF16_PARTIALS: the same launches, the partial outputs written and
+    merged as bf16 (half the workspace, half the merge's partial reads)."""
+    nbytes = slope.cp_prefill_workspace_size(w.S, w.Hq, w.dv, n, w.layout, sizes, bf16_partials=True)
+    ws16 = torch.empty((nbytes,), dtype=torch.uint8, device="cuda")
+
+    def step():
+        slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window, out=out, lse=lse, workspace=ws16,
+                         bf16_partials=True)
+
+    ms, world = time_variant(torch, step, stream, args, barrier, dist)
     return {"value": job_tflops(workload_flops(w, window), args.steps, world, ms), "unit": UNIT,
             "ms_per_step": ms / args.steps, "api": "slope_cp_prefill_ex(SLOPE_CP_BF16_PARTIALS)",
             "workspace_bytes": nbytes}
+
+
+def run_ulysses(slope, torch, w, window, q, k, v, out, lse, stream, args, barrier, dist):
+    """The same attention in the head-sharded (Ulysses) layout at the largest degree GQA allows
+    (one KV head per rank): every rank's whole-sequence attention of its head group, no merge."""
+    U = w.Hkv if w.Hkv <= 32 else 32
+    while w.Hkv % U:
+        U -= 1
+    nbytes = slope.cp_prefill_workspace_size(w.S, w.Hq, w.dv, U, "ulysses")
+    wsu = torch.empty((nbytes,), dtype=torch.uint8, device="cuda")
+
+    def step():
+        slope.cp_prefill(q, k, v, U, "ulysses", window=window, out=out, lse=lse, workspace=wsu)
+
+    ms, world = time_variant(torch, step, stream, args, barrier, dist)
+    return {"value": job_tflops(workload_flops(w, window), args.steps, world, ms), "unit": UNIT,
+            "ms_per_step": ms / args.steps, "api": f"slope_cp_prefill(SLOPE_LAYOUT_ULYSSES, n_chunks={U})",
+            "ranks": U, "gpu_launches_per_step": (U + 31) // 32}
 
 
 def run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier, dist):

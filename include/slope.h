@@ -86,7 +86,8 @@ typedef struct {
 typedef enum {
   SLOPE_LAYOUT_CONTIGUOUS = 0, /* ring of n ranks, rank r owns tokens [r*S/n, (r+1)*S/n)          */
   SLOPE_LAYOUT_ZIGZAG = 1,     /* ring of n ranks, rank r owns sub-chunks r and 2n-1-r of S/(2n)  */
-  SLOPE_LAYOUT_CHUNKED = 2     /* chunked prefill: chunk c attends to all earlier tokens + itself */
+  SLOPE_LAYOUT_CHUNKED = 2,    /* chunked prefill: chunk c attends to all earlier tokens + itself */
+  SLOPE_LAYOUT_ULYSSES = 3     /* n ranks, rank u owns every token of query-head group u of n     */
 } slope_layout;
 
 /*
@@ -150,11 +151,23 @@ SLOPE_API slope_status slope_lse_merge(const slope_tensor* outs, const slope_ten
  *     Chunk [s, e) yields two partials - against keys [0, s) and, causally,
  *     against [s, e) - computed chunk by chunk, in order (consecutive chunks
  *     sharing a launch up to 32 work items), then merged.
+ *   layout SLOPE_LAYOUT_ULYSSES: the head-sharded scheme (Moreh, section
+ *     "Introduction to Context Parallelism": an all-to-all hands each device
+ *     all tokens of a subset of the heads).  Rank u of n_chunks holds query
+ *     heads [u*Hq/n, (u+1)*Hq/n) and key/value heads [u*Hkv/n, (u+1)*Hkv/n) of
+ *     every token and computes their whole attention; there are no partials
+ *     and no merge: the ranks' items (one each, consecutive ranks sharing a
+ *     launch up to 32) write out and lse directly.  Hkv % n_chunks == 0 (GQA
+ *     limits the Ulysses degree to the number of key/value heads, as the page
+ *     notes), else SLOPE_ERR_LAYOUT; 1 <= n_chunks <= 32.  A bf16 out then
+ *     needs row/head strides that are multiples of 8 elements and a 16-byte
+ *     aligned pointer.
  *   causal, window, scale: as above.  out: bf16 or fp32 [S, Hq, dv];
  *   lse: fp32 [Hq, S] or NULL.
  *   workspace: device buffer of at least slope_cp_prefill_workspace_size()
  *     bytes, 256-byte aligned; it holds the fp32 partials between the
- *     attention launches and the merge.
+ *     attention launches and the merge (for ULYSSES only an lse plane, used
+ *     when lse is NULL).
  */
 SLOPE_API slope_status slope_cp_prefill(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
                               slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
@@ -296,6 +309,8 @@ typedef struct {
   int32_t n_kv;       /* number of key/value ranges (0..2)                 */
   int64_t kv_row0[2]; /* first key row of each range                       */
   int64_t kv_len[2];  /* length of each range                              */
+  int32_t head_group;    /* the entry covers query heads [g*Hq/n, (g+1)*Hq/n)  */
+  int32_t n_head_groups; /* n: 1 (all heads) except in SLOPE_LAYOUT_ULYSSES    */
 } slope_plan_item;
 
 /*

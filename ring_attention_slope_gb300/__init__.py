@@ -27,7 +27,7 @@ __all__ = [
     "cp_prefill_static_scratch",
 ]
 
-LAYOUTS = {"contiguous": 0, "zigzag": 1, "chunked": 2}
+LAYOUTS = {"contiguous": 0, "zigzag": 1, "chunked": 2, "ulysses": 3}
 _BF16, _F32 = 0, 1
 
 
@@ -39,7 +39,7 @@ class SlopeTensor(ctypes.Structure):
 class SlopePlanItem(ctypes.Structure):
     _fields_ = [("launch", ctypes.c_int32), ("plane", ctypes.c_int32), ("q_row0", ctypes.c_int64),
                 ("q_len", ctypes.c_int64), ("n_kv", ctypes.c_int32), ("kv_row0", ctypes.c_int64 * 2),
-                ("kv_len", ctypes.c_int64 * 2)]
+                ("kv_len", ctypes.c_int64 * 2), ("head_group", ctypes.c_int32), ("n_head_groups", ctypes.c_int32)]
 
 
 class SlopeError(RuntimeError):
@@ -376,7 +376,8 @@ def cp_prefill_plan(S, n_chunks, layout, *, chunk_sizes=None, causal=True, windo
     res = []
     for it in items[:n]:
         res.append({"launch": it.launch, "plane": it.plane, "q_row0": it.q_row0, "q_len": it.q_len,
-                    "kv": [(it.kv_row0[r], it.kv_len[r]) for r in range(it.n_kv)]})
+                    "kv": [(it.kv_row0[r], it.kv_len[r]) for r in range(it.n_kv)],
+                    "head_group": it.head_group, "n_head_groups": it.n_head_groups})
     return res, nl.value, npl.value
 
 

@@ -154,11 +154,13 @@ struct PItem {
   int64_t q_row0, q_len;
   int n_kv;
   Range kv[kMaxKvRanges];
+  int hg = 0, n_hg = 1;  // query heads [hg*Hq/n_hg, (hg+1)*Hq/n_hg)
 };
 struct Plan {
   std::vector<PItem> items;  // grouped by launch, in launch order
   int n_launches = 0;
   int n_planes = 0;
+  bool direct = false;  // the items write the final output (no partials, no merge)
 };
 
 // Restricts keys [k0, k1) to those some query in [q0, q1) can see (positions = rows).
@@ -195,7 +197,9 @@ slope_status chunk_list(int64_t S, int n_chunks, const int64_t* chunk_sizes, std
 // Ring layouts: at step t rank r holds the keys/values of rank (r - t) mod N; each
 // of r's query sub-chunks attends to the visible parts of those sub-chunks and
 // writes partial plane t.  Chunked: chunk [s, e) gives (Q_c, KV[0, s)) -> plane 0
-// and (Q_c, KV[s, e)) -> plane 1, one launch per chunk.
+// and (Q_c, KV[s, e)) -> plane 1, one launch per chunk.  Ulysses: after the
+// all-to-all, rank u holds every token of head group u of N and computes the whole
+// attention of those heads: one item per rank, written as the final output.
 slope_status build_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
                         int64_t window, Plan& plan) {
   plan = Plan();
@@ -264,27 +268,48 @@ slope_status build_plan(int64_t S, int n_chunks, slope_layout layout, const int6
     plan.n_planes = 2;
     return SLOPE_OK;
   }
+  if (layout == SLOPE_LAYOUT_ULYSSES) {
+    const int N = n_chunks;
+    if (N < 1 || N > kMaxRanks) return SLOPE_ERR_LAYOUT;
+    for (int u = 0; u < N; ++u) {
+      PItem it{};
+      it.launch = u;
+      it.plane = 0;
+      it.q_row0 = 0;
+      it.q_len = S;
+      it.hg = u;
+      it.n_hg = N;
+      int64_t k0 = 0, k1 = S;
+      if (trim(0, S, k0, k1, causal, window)) it.kv[it.n_kv++] = Range{k0, k1 - k0};
+      plan.items.push_back(it);
+    }
+    plan.n_launches = N;
+    plan.n_planes = 1;
+    plan.direct = true;
+    return SLOPE_OK;
+  }
   return SLOPE_ERR_LAYOUT;
 }
 
-// Rough work estimate (visible pairs) used to order items heaviest first.
+// Rough work estimate (visible pairs x share of the heads) used to order items heaviest first.
 double item_work(const PItem& it, int causal) {
   double w = 0;
   for (int r = 0; r < it.n_kv; ++r) {
     const bool diag = causal && it.kv[r].row0 + it.kv[r].len > it.q_row0;
     w += static_cast<double>(it.q_len) * static_cast<double>(it.kv[r].len) * (diag ? 0.5 : 1.0);
   }
-  return w;
+  return w / it.n_hg;
 }
 
-// Packs items into launch parameter blocks (<= kMaxItems each), heaviest first.
-void pack_items(std::vector<PItem> items, int causal, std::vector<std::vector<WorkItem>>& out) {
+// Packs items into launch parameter blocks (<= kMaxItems each), heaviest first.  Returns
+// false if a block has more work tiles than a launch indexes (2^31 - 1).
+bool pack_items(std::vector<PItem> items, int causal, int64_t Hq, std::vector<std::vector<WorkItem>>& out) {
   std::stable_sort(items.begin(), items.end(),
                    [&](const PItem& a, const PItem& b) { return item_work(a, causal) > item_work(b, causal); });
   out.clear();
   for (size_t i = 0; i < items.size(); i += kMaxItems) {
     std::vector<WorkItem> group;
-    int32_t begin = 0;
+    int64_t begin = 0;
     for (size_t j = i; j < std::min(items.size(), i + kMaxItems); ++j) {
       const PItem& s = items[j];
       WorkItem w{};
@@ -296,12 +321,16 @@ void pack_items(std::vector<PItem> items, int causal, std::vector<std::vector<Wo
       for (int r = 0; r < s.n_kv; ++r) w.kv[r] = KvRange{static_cast<int32_t>(s.kv[r].row0),
                                                         static_cast<int32_t>(s.kv[r].len)};
       w.n_blocks = static_cast<int32_t>((s.q_len + kRowsPerCta - 1) / kRowsPerCta);
-      w.cta_begin = begin;
-      begin += w.n_blocks;
+      w.h_begin = static_cast<int32_t>(s.hg * (Hq / s.n_hg));
+      w.h_count = static_cast<int32_t>(Hq / s.n_hg);
+      w.tile_begin = static_cast<int32_t>(begin);
+      begin += static_cast<int64_t>(w.n_blocks) * w.h_count;
+      if (begin > 0x7fffffffLL) return false;
       group.push_back(w);
     }
     out.push_back(std::move(group));
   }
+  return true;
 }
 
 // ---------------------------------------------------------------- launches
@@ -344,10 +373,12 @@ struct WorkspaceLayout {
   size_t out_bytes, lse_offset, total;
 };
 // Partial planes (fp32, or bf16 under SLOPE_CP_BF16_PARTIALS), then the fp32 lse planes.
-WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t dv, int n_planes, unsigned flags) {
+// A direct plan (Ulysses) keeps no partials: the workspace holds only an lse plane,
+// written when the caller passes no lse.
+WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t dv, int n_planes, unsigned flags, bool direct) {
   WorkspaceLayout w;
   const size_t elem = (flags & SLOPE_CP_BF16_PARTIALS) ? 2 : sizeof(float);
-  w.out_bytes = static_cast<size_t>(S) * Hq * dv * elem;
+  w.out_bytes = direct ? 0 : static_cast<size_t>(S) * Hq * dv * elem;
   w.lse_offset = round_up(w.out_bytes * n_planes, 256);
   w.total = w.lse_offset + round_up(static_cast<size_t>(S) * Hq * sizeof(float) * n_planes, 256);
   return w;
@@ -373,7 +404,13 @@ slope_status cp_prefill_check(const slope_tensor* q, const slope_tensor* k, cons
   if (S == 0) return SLOPE_ERR_SHAPE;
   if ((st = build_plan(S, n_chunks, layout, chunk_sizes, causal, window, plan)) != SLOPE_OK) return st;
   if (plan.n_planes > kMaxMerge) return SLOPE_ERR_UNSUPPORTED;
-  const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes, flags);
+  if (plan.direct) {
+    // whole KV heads per Ulysses rank; the attention kernel then writes out itself (bf16 16 bytes at a time)
+    if (Hkv % n_chunks != 0) return SLOPE_ERR_LAYOUT;
+    if (out->dtype == SLOPE_BF16 && (out->stride[0] % 8 || out->stride[1] % 8 || !aligned(out->data, 16)))
+      return SLOPE_ERR_STRIDE;
+  }
+  const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes, flags, plan.direct);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < wl.total) return SLOPE_ERR_WORKSPACE;
   return SLOPE_OK;
 }
@@ -389,7 +426,7 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
     return st;
   const int64_t S = q->shape[0], Hq = q->shape[1], dqk = q->shape[2];
   const int64_t Hkv = k->shape[1], dv = v->shape[2];
-  const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes, flags);
+  const WorkspaceLayout wl = workspace_layout(S, Hq, dv, plan.n_planes, flags, plan.direct);
   const bool bf16_partials = (flags & SLOPE_CP_BF16_PARTIALS) != 0;
   int* status = device_status_ptr();
   if (status == nullptr) return cuda_fail("device status word (cudaGetSymbolAddress)");
@@ -419,10 +456,29 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   base.status = status;
   base.wait_limit_ns = wait_limit_ns();
   CUtensorMap to;
-  base.out_plane_rows = S;
-  base.out_bf16 = bf16_partials ? 1 : 0;
-  base.out_tma =
-      make_out_map(&to, planes, bf16_partials, static_cast<int64_t>(plan.n_planes) * S, Hq, dv, Hq * dv, dv) ? 1 : 0;
+  if (plan.direct) {
+    // the items write the final out (and lse, else the workspace's lse plane) themselves
+    base.write_empty_out = 1;
+    base.out = static_cast<float*>(out->data);
+    base.out_srow = out->stride[0];
+    base.out_shead = out->stride[1];
+    base.out_splane = 0;
+    base.out_plane_rows = 0;
+    base.out_bf16 = out->dtype == SLOPE_BF16 ? 1 : 0;
+    base.out_tma =
+        make_out_map(&to, out->data, base.out_bf16 != 0, S, Hq, dv, out->stride[0], out->stride[1]) ? 1 : 0;
+    if (lse != nullptr) {
+      base.lse = static_cast<float*>(lse->data);
+      base.lse_srow = lse->stride[1];
+      base.lse_shead = lse->stride[0];
+    }
+    base.lse_splane = 0;
+  } else {
+    base.out_plane_rows = S;
+    base.out_bf16 = bf16_partials ? 1 : 0;
+    base.out_tma =
+        make_out_map(&to, planes, bf16_partials, static_cast<int64_t>(plan.n_planes) * S, Hq, dv, Hq * dv, dv) ? 1 : 0;
+  }
   if (!base.out_tma) to = tq;  // never used
 
   // A plane none of whose items sees a key (ring steps that a sliding window leaves
@@ -452,12 +508,13 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
       i = j;
     }
     if (items.empty()) continue;
-    pack_items(items, causal, groups);
+    if (!pack_items(items, causal, Hq, groups)) return SLOPE_ERR_UNSUPPORTED;
     for (const auto& g : groups)
       if ((st = run_attention(g, static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, to, base, tm, stream)) !=
           SLOPE_OK)
         return st;
   }
+  if (plan.direct) return SLOPE_OK;
 
   MergeParams mp{};
   mp.n = 0;
@@ -653,7 +710,7 @@ slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, co
     if (trim(q_off, q_off + Sq, k0, k1, causal, window)) it.kv[it.n_kv++] = Range{k0 - kv_off, k1 - k0};
   }
   std::vector<std::vector<WorkItem>> groups;
-  pack_items({it}, causal, groups);
+  if (!pack_items({it}, causal, Hq, groups)) return SLOPE_ERR_UNSUPPORTED;
 
   AttnParams base{};
   base.Hq = static_cast<int32_t>(Hq);
@@ -729,7 +786,7 @@ size_t slope_cp_prefill_workspace_size_ex(int64_t S, int64_t Hq, int64_t dv, int
   if (flags & ~static_cast<unsigned>(SLOPE_CP_BF16_PARTIALS)) return 0;
   Plan plan;
   if (build_plan(S, n_chunks, layout, chunk_sizes, 1, 0, plan) != SLOPE_OK) return 0;
-  return workspace_layout(S, Hq, dv, plan.n_planes, flags).total;
+  return workspace_layout(S, Hq, dv, plan.n_planes, flags, plan.direct).total;
 }
 
 size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t dv, int n_chunks, slope_layout layout,
@@ -885,6 +942,8 @@ int64_t slope_cp_prefill_plan(int64_t S, int n_chunks, slope_layout layout, cons
       o.kv_row0[r] = p.kv[r].row0;
       o.kv_len[r] = p.kv[r].len;
     }
+    o.head_group = p.hg;
+    o.n_head_groups = p.n_hg;
   }
   if (n_launches != nullptr) *n_launches = plan.n_launches;
   if (n_planes != nullptr) *n_planes = plan.n_planes;

@@ -212,11 +212,12 @@ struct Tile {
 // `ii` carries the item index from the caller's previous work tile: a CTA visits its
 // tiles in increasing w, so the item index never decreases and the scan resumes there.
 __device__ __forceinline__ void decode_tile(const AttnParams& p, const WorkItem* items, int w, Tile& T, int& ii) {
-  while (ii < p.n_items - 1 && w >= (items[ii].cta_begin + items[ii].n_blocks) * p.Hq) ++ii;
+  while (ii < p.n_items - 1 && w >= items[ii].tile_begin + items[ii].n_blocks * items[ii].h_count) ++ii;
   T.itm = items[ii];
-  const int local = w - T.itm.cta_begin * p.Hq;
-  T.blk = T.itm.n_blocks - 1 - local / p.Hq;
-  T.h = local % p.Hq;
+  const int hc = T.itm.h_count;
+  const int local = w - T.itm.tile_begin;
+  T.blk = T.itm.n_blocks - 1 - local / hc;
+  T.h = T.itm.h_begin + local % hc;
   T.g = T.h / p.group;
 #pragma unroll
   for (int t = 0; t < kQTiles; ++t) {
@@ -872,7 +873,7 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   using C = K1Cfg<DQK, DV>;
   if (p.n_items <= 0) return cudaSuccess;
   const WorkItem& last = p.items[p.n_items - 1];
-  const long long tiles = static_cast<long long>(last.cta_begin + last.n_blocks) * p.Hq;
+  const long long tiles = static_cast<long long>(last.tile_begin) + static_cast<long long>(last.n_blocks) * last.h_count;
   if (tiles <= 0) return cudaSuccess;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   p.total_tiles = static_cast<int32_t>(tiles);

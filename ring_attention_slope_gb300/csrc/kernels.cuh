@@ -22,22 +22,26 @@ struct KvRange {
   int32_t len;   // keys in the range
 };
 
-// One query block and the key/value ranges it attends to in this launch.
+// One query block of a range of query heads, and the key/value ranges it attends to in
+// this launch.  Its work tiles are (row block, head) pairs, row blocks from the last one
+// down and heads inner.
 struct WorkItem {
-  int32_t q_row0;     // first query row (in q)
-  int32_t q_len;      // query rows
-  int32_t out_row0;   // output row of q_row0
-  int32_t plane;      // output plane
-  int32_t n_kv;       // 0..kMaxKvRanges
-  int32_t cta_begin;  // first CTA-row-block of this item (prefix sum over items)
-  int32_t n_blocks;   // ceil(q_len / kRowsPerCta)
+  int32_t q_row0;      // first query row (in q)
+  int32_t q_len;       // query rows
+  int32_t out_row0;    // output row of q_row0
+  int32_t plane;       // output plane
+  int32_t n_kv;        // 0..kMaxKvRanges
+  int32_t tile_begin;  // first work tile of this item (prefix sum over items of n_blocks * h_count)
+  int32_t n_blocks;    // ceil(q_len / kRowsPerCta)
+  int32_t h_begin;     // first query head
+  int32_t h_count;     // query heads (whole KV-head groups)
   KvRange kv[kMaxKvRanges];
 };
 static_assert(sizeof(WorkItem) % 4 == 0, "work items are copied as 32-bit words");
 
 struct AttnParams {
   int32_t n_items;
-  int32_t total_tiles;      // work tiles (item row blocks x query heads); set by the launcher
+  int32_t total_tiles;      // work tiles (sum over items of row blocks x heads); set by the launcher
   int32_t Hq;
   int32_t group;            // Hq / Hkv
   int32_t causal;

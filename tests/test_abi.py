@@ -82,6 +82,13 @@ def test_cp_prefill_argument_errors(lib):
     assert _cp(lib, q, k, v, _t([S, Hq, 32]), lse) == E_SHAPE                         # out dv
     assert _cp(lib, q, k, v, out, _t([S, Hq], dtype=1)) == E_SHAPE                    # lse transposed
     assert _cp(lib, q, k, v, out, lse, window=-1) == E_SHAPE
+    # Ulysses: whole KV heads per rank (Hkv % n == 0); direct bf16 output needs 8-element strides
+    q8, k2, v2, out8 = _t([S, 8, d]), _t([S, 2, d]), _t([S, 2, d]), _t([S, 8, d])
+    lse8 = _t([8, S], dtype=1)
+    assert _cp(lib, q8, k2, v2, out8, lse8, n=4, layout=3) == E_LAYOUT                # 2 KV heads, 4 ranks
+    assert _cp(lib, q8, k2, v2, out8, lse8, n=2, layout=3, ws=0) == E_WS
+    assert _cp(lib, q8, k2, v2, _t([S, 8, d], stride=[8 * d + 4, d, 1]), lse8, n=2, layout=3) == E_STRIDE
+    assert _cp(lib, q8, k2, v2, out8, lse8, n=33, layout=3) == E_LAYOUT
 
 
 def test_attn_partial_and_merge_argument_errors(lib):
@@ -147,6 +154,8 @@ def test_workspace_size(lib):
     wc = slope.cp_prefill_workspace_size(65536, 64, 64, 6, "chunked", [12288] * 5 + [4096])
     assert wc >= 2 * 65536 * 64 * 65 * 4
     assert slope.cp_prefill_workspace_size(1000, 4, 64, 8, "zigzag") == 0
+    # Ulysses keeps no partials: only an lse plane (for calls without lse)
+    assert slope.cp_prefill_workspace_size(1000, 4, 64, 2, "ulysses") == (1000 * 4 * 4 + 255) // 256 * 256
     assert slope.cp_prefill_workspace_size(1024, 4, 96, 4, "zigzag") == 0
 
 

@@ -464,3 +464,57 @@ def test_cp_prefill_bf16_partials_are_the_fp32_partials_rounded(layout, n, windo
 
 def test_full_causal_gqa_s32k_zigzag8_bf16_partials():
     check_full_workload(wl.WORKLOADS[1], 0, rows_random=2048, bf16_partials=True)
+
+
+# ---------------------------------------------------------------- Ulysses head-sharded layout
+
+@pytest.mark.parametrize("S,Hq,Hkv,dqk,dv,U,window", [
+    (2048, 8, 4, 64, 64, 4, 0), (2048, 8, 4, 64, 64, 2, 100), (1000, 8, 2, 128, 128, 2, 0),
+    (1536, 4, 4, 192, 128, 4, 0), (777, 6, 3, 64, 64, 3, 37), (2048, 8, 4, 64, 64, 1, 0)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_cp_prefill_ulysses_matches_oracle_and_fused(S, Hq, Hkv, dqk, dv, U, window, out_dtype):
+    """Each Ulysses rank computes the whole attention of its head group: the result matches the
+    oracle and is bit-identical to the single launch over all heads (the same tiles, listed per
+    head group)."""
+    q, k, v = qkv(S, Hq, Hkv, dqk, dv, seed=61 + U + dqk, scale_v=0.7)
+    out, lse = slope.cp_prefill(q, k, v, U, "ulysses", window=window, out_dtype=out_dtype)
+    ref_o = torch.empty_like(out)
+    ref_l = torch.empty_like(lse)
+    slope.attn_partial(q, k, v, causal=True, window=window, out=ref_o, lse=ref_l)
+    torch.cuda.synchronize()
+    assert slope.device_status() == (0, 0)
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, window=window)
+    compare(out.float().cpu(), lse.cpu(), ro, rl, f"ulysses U={U} W={window} {out_dtype}")
+
+
+def test_cp_prefill_ulysses_strided_out_and_no_lse():
+    """A padded fp32 out (the row/head strides of a wider buffer; the padding stays untouched) and
+    no lse (the kernel writes the workspace's lse plane instead)."""
+    S, Hq, Hkv, d, U = 1024, 8, 4, 64, 4
+    q, k, v = qkv(S, Hq, Hkv, d, d, seed=71)
+    big = torch.full((S, Hq, d + 4), 7.0, dtype=torch.float32, device="cuda")
+    out = big[:, :, :d]
+    ws = torch.empty((slope.cp_prefill_workspace_size(S, Hq, d, U, "ulysses"),), dtype=torch.uint8, device="cuda")
+    o, l = slope.cp_prefill(q, k, v, U, "ulysses", out=out, workspace=ws, want_lse=False)
+    torch.cuda.synchronize()
+    assert l is None and o.data_ptr() == big.data_ptr()
+    assert torch.all(big[:, :, d:] == 7.0)  # the padding is untouched
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True)
+    lse_ws = ws[:S * Hq * 4].view(torch.float32).view(S, Hq).T.cpu()  # [S, Hq] plane, head fastest
+    compare(out.cpu(), lse_ws, ro, rl, "ulysses strided out, lse in the workspace")
+
+
+def test_full_causal_gqa_s32k_ulysses8():
+    """The 32K GQA workload (8 KV heads) as 8 Ulysses ranks, sampled rows of one KV group."""
+    w = wl.WORKLOADS[1]
+    q, k, v = wl.workload_qkv(w, device="cuda")
+    out, lse = slope.cp_prefill(q, k, v, 8, "ulysses")
+    torch.cuda.synchronize()
+    assert slope.device_status() == (0, 0)
+    rows = wl.sample_rows(w, n_random=2048)
+    heads = wl.sample_heads(w)
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, rows=rows, heads=heads)
+    og = out[torch.from_numpy(rows).cuda()][:, heads].float().cpu()
+    lg = lse[heads][:, torch.from_numpy(rows).cuda()].cpu()
+    compare(og, lg, ro, rl, "s32k ulysses8")

@@ -1,5 +1,6 @@
-"""Host-side work decomposition: ring steps (zigzag / contiguous) and chunked
-prefill items cover every visible (query, key) pair exactly once."""
+"""Host-side work decomposition: ring steps (zigzag / contiguous), chunked
+prefill items and Ulysses head groups cover every visible (query, key, head)
+triple exactly once."""
 import numpy as np
 import pytest
 
@@ -110,3 +111,32 @@ def test_plan_errors():
         slope.cp_prefill_plan(1000, 8, "zigzag")
     with pytest.raises(slope.SlopeError):
         slope.cp_prefill_plan(1000, 2, "chunked", chunk_sizes=[400, 500])
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 32])
+@pytest.mark.parametrize("window", [0, 1, 37])
+def test_ulysses_plan_covers_each_head_and_visible_pair_once(N, window):
+    """Rank u owns head group u of N over every token; together the ranks cover every
+    (head, visible pair) once, with one item per rank, no partial plane and no merge."""
+    S, Hq = 200, 64
+    items, n_launches, n_planes = slope.cp_prefill_plan(S, N, "ulysses", window=window)
+    assert n_launches == N and n_planes == 1 and len(items) == N
+    cnt_heads = np.zeros((Hq, S, S), dtype=np.int32)
+    vis = visible(S, window)
+    for it in items:
+        assert it["n_head_groups"] == N and it["plane"] == 0 and it["launch"] == it["head_group"]
+        assert it["q_row0"] == 0 and it["q_len"] == S
+        h0, h1 = it["head_group"] * Hq // N, (it["head_group"] + 1) * Hq // N
+        cnt, _ = coverage([it], S, window)
+        cnt_heads[h0:h1] += cnt
+    assert np.array_equal(cnt_heads, np.broadcast_to(vis.astype(np.int32), cnt_heads.shape))
+    # every other layout lists all heads in every entry
+    for layout, n in (("zigzag", 4), ("chunked", 3)):
+        its, _, _ = slope.cp_prefill_plan(240, n, layout)
+        assert all(it["head_group"] == 0 and it["n_head_groups"] == 1 for it in its)
+
+
+def test_ulysses_plan_errors():
+    for N in (0, 33):
+        with pytest.raises(slope.SlopeError):
+            slope.cp_prefill_plan(256, N, "ulysses")
