@@ -315,14 +315,17 @@ def run_gpu(args, w):
     k2_gbs = merge_bytes * k2_n / (k2_ms * 1e-3) / 1e9 if k2_ms > 0 else None
 
     # ---- the same attention as one launch (bf16 out, no partials, no merge): the fused single-GPU form
-    fused = run_fused(slope, torch, w, window, q, k, v, stream, args, barrier, dist)
+    fused = None if args.no_variants else run_fused(slope, torch, w, window, q, k, v, stream, args, barrier, dist)
 
     # ---- the same step with the partials kept in bf16 between the attention launches and the merge
-    bf16p = run_bf16_partials(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream, args, barrier, dist)
-    bf16p["gpu_launches_per_step"] = counts[0]  # the same launches as the fp32-partial step
+    bf16p = None
+    if not args.no_variants:
+        bf16p = run_bf16_partials(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream, args, barrier, dist)
+        bf16p["gpu_launches_per_step"] = counts[0]  # the same launches as the fp32-partial step
 
     # ---- the same attention in the head-sharded (Ulysses) layout
-    ulysses = run_ulysses(slope, torch, w, window, q, k, v, out, lse, stream, args, barrier, dist)
+    ulysses = None if args.no_variants else run_ulysses(slope, torch, w, window, q, k, v, out, lse, stream, args,
+                                                         barrier, dist)
 
     # ---- end to end through the public call with pinned host buffers
     e2e = None if args.no_e2e else run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier,
@@ -530,6 +533,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the fused, bf16-partial and Ulysses legs (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -97,6 +97,10 @@ struct K1Cfg {
   // overwrites S (dv = 128).  Measured (kernel TFLOP/s): MLA shape 192/128 1141 -> 1220
   // with turns; at dv = 64 turns cost more than they save (causal 32K zigzag 956 -> 920).
   static constexpr bool kTurns = !kSepP;
+  // Head-grouped tile order (see tile_head_group) for the wider head sizes, where MLA-shaped
+  // attention (one query head per KV head) runs; at d = 64 the ungrouped decode is kept, which
+  // measured 2% faster on the GQA workloads (where grouping would not change the order).
+  static constexpr bool kGroupedTiles = DQK >= 128;
 };
 
 __device__ __forceinline__ int floor_div(int a, int b) {
@@ -211,13 +215,25 @@ struct Tile {
 // later (heavier under the causal mask) row blocks before its earlier ones.
 // `ii` carries the item index from the caller's previous work tile: a CTA visits its
 // tiles in increasing w, so the item index never decreases and the scan resumes there.
+// kGrouped: tiles run head group by head group (p.head_group heads each); otherwise every
+// head of an item is inner to its row blocks (p.head_group is then the item's h_count).
+template <bool kGrouped>
 __device__ __forceinline__ void decode_tile(const AttnParams& p, const WorkItem* items, int w, Tile& T, int& ii) {
   while (ii < p.n_items - 1 && w >= items[ii].tile_begin + items[ii].n_blocks * items[ii].h_count) ++ii;
   T.itm = items[ii];
-  const int hc = T.itm.h_count;
   const int local = w - T.itm.tile_begin;
-  T.blk = T.itm.n_blocks - 1 - local / hc;
-  T.h = T.itm.h_begin + local % hc;
+  if constexpr (kGrouped) {
+    const int hg = p.head_group;
+    const int per_group = T.itm.n_blocks * hg;
+    const int grp = local / per_group;
+    const int rem = local - grp * per_group;
+    T.blk = T.itm.n_blocks - 1 - rem / hg;
+    T.h = T.itm.h_begin + grp * hg + rem % hg;
+  } else {
+    const int hc = T.itm.h_count;
+    T.blk = T.itm.n_blocks - 1 - local / hc;
+    T.h = T.itm.h_begin + local % hc;
+  }
   T.g = T.h / p.group;
 #pragma unroll
   for (int t = 0; t < kQTiles; ++t) {
@@ -312,7 +328,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       int item_hint = 0;
       for (int w = blockIdx.x; w < total; w += gridDim.x) {
         Tile T;
-        decode_tile(p, sItems, w, T, item_hint);
+        decode_tile<C::kGroupedTiles>(p, sItems, w, T, item_hint);
         if (!has_steps(T.itm, p, T.geo)) continue;
         // Q of the previous work tile is in use until its last S MMAs are done
         if (wt > 0 && !wait_bounded(bar_qempty, (wt - 1) & 1, cta_abort, p.status, limit, 11)) {
@@ -428,7 +444,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       int item_hint = 0;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         Tile T;
-        decode_tile(p, sItems, w, T, item_hint);
+        decode_tile<C::kGroupedTiles>(p, sItems, w, T, item_hint);
         if (!has_steps(T.itm, p, T.geo)) continue;
         if (!wait_bounded(bar_q, wt & 1, cta_abort, p.status, limit, 3)) {
           ok = false;
@@ -526,7 +542,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     int item_hint = 0;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       Tile T;
-      decode_tile(p, sItems, w, T, item_hint);
+      decode_tile<C::kGroupedTiles>(p, sItems, w, T, item_hint);
       const int rows_t = t == 0 ? T.geo.rows[0] : T.geo.rows[1];
       // turns of this work tile: the step count of the tile with more steps
       int n_turns = 0;
@@ -867,6 +883,36 @@ int resident_ctas() {
   return sms;
 }
 
+int gcd_int(int a, int b) {
+  while (b != 0) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+// Query heads per tile group.  With every head of an item inner to its row blocks, the
+// resident CTAs work on about grid / heads row blocks at a time.  When a KV head serves few
+// query heads (Hq / Hkv < 4, as in MLA-shaped attention), that is about one CTA per KV head,
+// so each CTA streams its own K/V tiles from DRAM.  A group of heads just large enough to
+// give the grid one group's row blocks puts many CTAs on the same heads, and they then share
+// those heads' K/V tiles in L2.  With larger GQA groups the query heads of a KV head already
+// share its tiles, and one group of all the heads is kept.
+int tile_head_group(const AttnParams& p, long long grid) {
+  int common = 0, max_blocks = 1;
+  for (int i = 0; i < p.n_items; ++i) {
+    common = gcd_int(common, p.items[i].h_count);
+    max_blocks = std::max(max_blocks, static_cast<int>(p.items[i].n_blocks));
+  }
+  if (common <= 0) return 1;
+  if (p.group >= 4) return common;
+  const long long want = (grid + max_blocks - 1) / max_blocks;
+  for (int hg = 1; hg < common; ++hg)
+    if (common % hg == 0 && hg >= want) return hg;
+  return common;
+}
+
 template <int DQK, int DV>
 cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                         AttnParams p, cudaStream_t stream) {
@@ -878,6 +924,7 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   p.total_tiles = static_cast<int32_t>(tiles);
   const long long grid = std::min<long long>(tiles, resident_ctas());
+  p.head_group = C::kGroupedTiles ? tile_head_group(p, grid) : 0;
   cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;

@@ -23,8 +23,9 @@ struct KvRange {
 };
 
 // One query block of a range of query heads, and the key/value ranges it attends to in
-// this launch.  Its work tiles are (row block, head) pairs, row blocks from the last one
-// down and heads inner.
+// this launch.  Its work tiles are (row block, head) pairs: head group by head group
+// (AttnParams::head_group heads each), and in a group row blocks from the last one down
+// with the group's heads inner.
 struct WorkItem {
   int32_t q_row0;      // first query row (in q)
   int32_t q_len;       // query rows
@@ -42,6 +43,8 @@ static_assert(sizeof(WorkItem) % 4 == 0, "work items are copied as 32-bit words"
 struct AttnParams {
   int32_t n_items;
   int32_t total_tiles;      // work tiles (sum over items of row blocks x heads); set by the launcher
+  int32_t head_group;       // query heads per tile group (divides every item's h_count; 0 = one group per
+                            // item); set by the launcher
   int32_t Hq;
   int32_t group;            // Hq / Hkv
   int32_t causal;

@@ -518,3 +518,24 @@ def test_full_causal_gqa_s32k_ulysses8():
     og = out[torch.from_numpy(rows).cuda()][:, heads].float().cpu()
     lg = lse[heads][:, torch.from_numpy(rows).cuda()].cpu()
     compare(og, lg, ro, rl, "s32k ulysses8")
+
+
+def test_head_grouped_tile_order_with_one_query_head_per_kv_head():
+    """With Hq / Hkv < 4 and dqk >= 128 the launch orders its tiles head group by head group (here 8 heads
+    per group over 32 row blocks for the single launch and for 4 Ulysses ranks, 1 per group for 32 ranks):
+    every (row block, head) is computed once, by the same arithmetic, whatever the grouping."""
+    S, H, d = 8192, 32, 128
+    q, k, v = qkv(S, H, H, d, d, seed=83, scale_v=0.6)
+    fo = torch.empty((S, H, d), dtype=torch.bfloat16, device="cuda")
+    fl = torch.empty((H, S), dtype=torch.float32, device="cuda")
+    slope.attn_partial(q, k, v, causal=True, out=fo, lse=fl)
+    res = [slope.cp_prefill(q, k, v, U, "ulysses") for U in (32, 4)]
+    torch.cuda.synchronize()
+    assert slope.device_status() == (0, 0)
+    for o, l in res:
+        assert torch.equal(o, fo) and torch.equal(l, fl)
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([np.arange(128), np.arange(S - 128, S), rng.integers(0, S, 384)]))
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, rows=rows)
+    rt = torch.from_numpy(rows).cuda()
+    compare(fo[rt].float().cpu(), fl[:, rt].cpu(), ro, rl, "head-grouped tile order")
