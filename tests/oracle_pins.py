@@ -348,5 +348,33 @@ def check_invariance():
             close(l, full_l, 1e-12, f"chunked {sizes} W={window} lse")
 
 
+def check_head_and_row_subsets():
+    """The oracle's row/head subsets (used on the large workloads) and the Ulysses split (each rank's
+    contiguous query-head group over all tokens, KV heads of that group) equal the matching slices of
+    the materialised attention; a subset head keeps its global KV head (h // G, not its index in the
+    subset)."""
+    S, Hq, Hkv, dqk, dv = 96, 8, 2, 16, 8
+    q, k, v = rand_qkv(S, Hq, Hkv, dqk, dv, seed=700, scale_v=1.1)
+    for window in (0, 17):
+        full_o, full_l = brute_numpy(q, k, v, causal=True, window=window)
+        for heads in ([4, 5, 6, 7], [1, 6], [7], [6, 1]):
+            for rows in (None, [0, 5, 95, 40]):
+                o, l = oracle.attention(q, k, v, causal=True, window=window, heads=heads, rows=rows)
+                r = np.arange(S) if rows is None else np.array(rows)
+                close(o, full_o[r][:, heads], 1e-12, f"heads {heads} rows {rows} W={window} out")
+                close(l, full_l[heads][:, r], 1e-12, f"heads {heads} rows {rows} W={window} lse")
+        for U in (1, 2):
+            hq, hk = Hq // U, Hkv // U
+            outs, lses = [], []
+            for u in range(U):
+                o, l = oracle.attention(q[:, u * hq:(u + 1) * hq], k[:, u * hk:(u + 1) * hk], v[:, u * hk:(u + 1) * hk],
+                                        causal=True, window=window)
+                outs.append(o)
+                lses.append(l)
+            close(np.concatenate(outs, axis=1), full_o, 1e-12, f"Ulysses U={U} W={window} out")
+            close(np.concatenate(lses, axis=0), full_l, 1e-12, f"Ulysses U={U} W={window} lse")
+
+
 ALL_CHECKS = [check_golden_attention, check_golden_merge, check_brute_python, check_brute_numpy,
-              check_torch_sdpa, check_closed_forms, check_merge_algebra, check_invariance]
+              check_torch_sdpa, check_closed_forms, check_merge_algebra, check_invariance,
+              check_head_and_row_subsets]

@@ -19,6 +19,8 @@ MUTANTS = {
     "diagonal_excluded": ("if (causal && pk > pq)", "if (causal && pk >= pq)"),
     "window_off_by_one": ("pq - pk >= window", "pq - pk > window"),
     "gqa_modulo_map": ("const int g = h / G;", "const int g = h % Hkv;"),
+    "subset_head_local_kv": ("const int g = h / G;", "const int g = (int)hr / G;"),
+    "subset_rows_ignored": ("const int64_t i = rows ? rows[rr] : rr;", "const int64_t i = rr;"),
     "scale_dropped": ("s[j] = scale * dot;", "s[j] = dot;"),
     "lse_log2": ("*ls = m + log(l);", "*ls = m + log2(l);"),
     "lse_unshifted": ("*ls = m + log(l);", "*ls = log(l);"),
