@@ -25,7 +25,9 @@ across the ring):
 Pins (tests under ``-m "not gpu"``): brute force on tiny inputs (pure-Python
 loops and a materialised numpy score matrix), torch's CPU scaled-dot-product
 attention in fp64 with an explicit mask, closed forms (zero keys, a single
-visible key, constant values), merge algebra and chunk-layout invariance.
+visible key, constant values), merge algebra, chunk-layout invariance, and
+row/head subsets (with the Ulysses head split) against the full materialised
+attention.
 """
 from __future__ import annotations
 
