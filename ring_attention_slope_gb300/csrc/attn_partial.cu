@@ -689,11 +689,9 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           ++taken;
         }
         const bool any_need = __any_sync(0xffffffffu, need);
-        if (!C::kSepP && any_need && nl > 0) {
-          // the previous PV of this tile must be done before O_t is rescaled
-          if (!warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 9))) return false;
-          tc_fence_after_sync();
-        }
+        // O_t holds the previous PV's result here.  Separate P: the P store above waited for
+        // that PV.  P inside S_t: the issuer sent S_t(n) only after PV(n-1) completed, and the
+        // commit behind bar_s tracks every earlier MMA of that issuer.
         if (any_need && nl > 0) {
 #pragma unroll 1
           for (int c = 0; c < DV / 16; ++c) {

@@ -59,6 +59,8 @@ WORKLOADS = [
 # Smaller case of the same shape family, for profiler captures (inputs still larger than L2).
 PROFILE_WORKLOADS = [
     Workload("profile_s16k_zigzag8", 16384, 64, 8, 64, 64, 0.5, "zigzag", 8, index=5),
+    Workload("profile_mla_s16k_d192_128_chunked", 16384, 128, 128, 192, 128, 0.3, "chunked", 0, index=6,
+             chunk_factor_lo=0.65),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_WORKLOADS}
 

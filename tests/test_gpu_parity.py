@@ -112,24 +112,26 @@ def test_attn_partial_matches_oracle(case):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_attn_partial_score_jumps_inside_a_key_tile(causal):
+@pytest.mark.parametrize("d,dv", [(64, 64), (128, 64), (128, 128), (192, 128)])
+def test_attn_partial_score_jumps_inside_a_key_tile(causal, d, dv):
     """Keys whose scores jump by tens of log2 units inside one 128-key tile and again in
     later tiles: the running max moves many times and the row sum and O are rescaled
-    by factors down to 2^-100 and below."""
-    S, Hq, Hkv, d = 640, 2, 1, 64
+    by factors down to 2^-100 and below (with P in its own TMEM columns at dv = 64 and
+    over S at dv = 128)."""
+    S, Hq, Hkv = 640, 2, 1
     g = torch.Generator().manual_seed(77)
     u = torch.randn(d, generator=g)
-    u = u / u.norm() * 8.0  # |u|^2 = 64: key a*u scores about 8a against q ~ u + noise
+    u = u / u.norm() * 8.0  # |u|^2 = 64: key a*u scores about 64a*scale against q ~ u + noise
     q = (torch.randn(S, Hq, d, generator=g) + u).to(torch.bfloat16)
     k = torch.randn(S, Hkv, d, generator=g) * 0.1
-    v = torch.randn(S, Hkv, d, generator=g)
+    v = torch.randn(S, Hkv, dv, generator=g)
     for j, a in [(40, 1.5), (70, 4.0), (100, 8.0), (170, 12.0), (300, 20.0), (333, 3.0), (520, 30.0)]:
         k[j, :] = a * u
     k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
     out, lse = slope.attn_partial(q.cuda(), k.cuda(), v.cuda(), causal=causal)
     torch.cuda.synchronize()
     ro, rl = oracle.attention(q, k, v, causal=causal)
-    compare(out.cpu(), lse.cpu(), ro, rl, f"score jumps causal={causal}")
+    compare(out.cpu(), lse.cpu(), ro, rl, f"score jumps causal={causal} d={d}/{dv}")
     assert slope.device_status() == (0, 0)
 
 
