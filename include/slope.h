@@ -91,6 +91,19 @@ typedef enum {
 } slope_layout;
 
 /*
+ * Ulysses x Ring: a layout word may carry a Ulysses degree u in bits 8-15 on top of
+ * SLOPE_LAYOUT_CONTIGUOUS, SLOPE_LAYOUT_ZIGZAG or SLOPE_LAYOUT_CHUNKED, e.g.
+ * SLOPE_LAYOUT_ZIGZAG | SLOPE_ULYSSES_DEGREE(4) (0 or 1: none).  The Moreh post
+ * ("Introduction to Context Parallelism") combines the two schemes: after the
+ * all-to-all each of u groups holds every token of its query-head group, and the
+ * ring (or the chunks) runs within each group.  Every ring step's (or chunk's)
+ * partial is then computed as u head-group items that write the same partial
+ * planes, so the result equals the layout without the degree.  u must divide Hkv
+ * (else SLOPE_ERR_LAYOUT), 2 <= u <= 32, and SLOPE_LAYOUT_ULYSSES takes none.
+ */
+#define SLOPE_ULYSSES_DEGREE(u) ((slope_layout)(((unsigned)(u) & 0xffu) << 8))
+
+/*
  * Partial attention of one query block against one key/value block
  * (Ring Attention item: a device attends its partial queries to the partial
  * keys/values it holds).

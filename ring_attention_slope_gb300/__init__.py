@@ -183,6 +183,13 @@ def _layout(layout):
     return int(layout)
 
 
+def layout_code(layout, ulysses=1):
+    """Layout word of the C ABI: a base layout (name or code) and, for the ring and chunked layouts,
+    a Ulysses degree (SLOPE_ULYSSES_DEGREE: the head groups of a Ulysses x Ring split)."""
+    code = _layout(layout)
+    return code | (int(ulysses) << 8) if int(ulysses) > 1 else code
+
+
 # ---------------------------------------------------------------- public calls
 
 def attn_partial(q, k, v, *, q_off=0, kv_off=0, causal=True, window=0, scale=0.0, out=None, lse=None,

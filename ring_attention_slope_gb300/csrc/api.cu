@@ -160,7 +160,8 @@ struct Plan {
   std::vector<PItem> items;  // grouped by launch, in launch order
   int n_launches = 0;
   int n_planes = 0;
-  bool direct = false;  // the items write the final output (no partials, no merge)
+  bool direct = false;     // the items write the final output (no partials, no merge)
+  int n_head_groups = 1;   // Ulysses degree (query-head groups); must divide Hkv
 };
 
 // Restricts keys [k0, k1) to those some query in [q0, q1) can see (positions = rows).
@@ -200,8 +201,8 @@ slope_status chunk_list(int64_t S, int n_chunks, const int64_t* chunk_sizes, std
 // and (Q_c, KV[s, e)) -> plane 1, one launch per chunk.  Ulysses: after the
 // all-to-all, rank u holds every token of head group u of N and computes the whole
 // attention of those heads: one item per rank, written as the final output.
-slope_status build_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
-                        int64_t window, Plan& plan) {
+slope_status build_base_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
+                             int64_t window, Plan& plan) {
   plan = Plan();
   if (S <= 0 || S > kMaxSeq) return SLOPE_ERR_SHAPE;
   if (window < 0) return SLOPE_ERR_SHAPE;
@@ -286,9 +287,40 @@ slope_status build_plan(int64_t S, int n_chunks, slope_layout layout, const int6
     plan.n_launches = N;
     plan.n_planes = 1;
     plan.direct = true;
+    plan.n_head_groups = N;
     return SLOPE_OK;
   }
   return SLOPE_ERR_LAYOUT;
+}
+
+// The layout word: the base layout in the low 8 bits and, for the ring and chunked layouts, a
+// Ulysses degree u in bits 8-15 (0 or 1: none).  Ulysses x Ring: each of the base plan's items
+// is split into u items, one per query-head group (the ranks of one Ulysses group after the
+// all-to-all), which write the same partial planes.
+slope_status build_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
+                        int64_t window, Plan& plan) {
+  const unsigned word = static_cast<unsigned>(layout);
+  if (word >> 16) return SLOPE_ERR_LAYOUT;
+  const slope_layout base = static_cast<slope_layout>(word & 0xffu);
+  const int u = static_cast<int>((word >> 8) & 0xffu);
+  slope_status st = build_base_plan(S, n_chunks, base, chunk_sizes, causal, window, plan);
+  if (st != SLOPE_OK || u <= 1) return st;
+  if (base == SLOPE_LAYOUT_ULYSSES || u > kMaxRanks) {
+    plan = Plan();
+    return SLOPE_ERR_LAYOUT;
+  }
+  std::vector<PItem> split;
+  split.reserve(plan.items.size() * static_cast<size_t>(u));
+  for (const PItem& it : plan.items)
+    for (int g = 0; g < u; ++g) {
+      PItem c = it;
+      c.hg = g;
+      c.n_hg = u;
+      split.push_back(c);
+    }
+  plan.items = std::move(split);
+  plan.n_head_groups = u;
+  return SLOPE_OK;
 }
 
 // Rough work estimate (visible pairs x share of the heads) used to order items heaviest first.
@@ -404,9 +436,9 @@ slope_status cp_prefill_check(const slope_tensor* q, const slope_tensor* k, cons
   if (S == 0) return SLOPE_ERR_SHAPE;
   if ((st = build_plan(S, n_chunks, layout, chunk_sizes, causal, window, plan)) != SLOPE_OK) return st;
   if (plan.n_planes > kMaxMerge) return SLOPE_ERR_UNSUPPORTED;
+  if (Hkv % plan.n_head_groups != 0) return SLOPE_ERR_LAYOUT;  // whole KV heads per Ulysses rank
   if (plan.direct) {
-    // whole KV heads per Ulysses rank; the attention kernel then writes out itself (bf16 16 bytes at a time)
-    if (Hkv % n_chunks != 0) return SLOPE_ERR_LAYOUT;
+    // the attention kernel writes out itself (bf16 16 bytes at a time)
     if (out->dtype == SLOPE_BF16 && (out->stride[0] % 8 || out->stride[1] % 8 || !aligned(out->data, 16)))
       return SLOPE_ERR_STRIDE;
   }

@@ -89,6 +89,9 @@ def test_cp_prefill_argument_errors(lib):
     assert _cp(lib, q8, k2, v2, out8, lse8, n=2, layout=3, ws=0) == E_WS
     assert _cp(lib, q8, k2, v2, _t([S, 8, d], stride=[8 * d + 4, d, 1]), lse8, n=2, layout=3) == E_STRIDE
     assert _cp(lib, q8, k2, v2, out8, lse8, n=33, layout=3) == E_LAYOUT
+    # Ulysses x Ring: the degree (bits 8-15 of the layout word) must divide Hkv
+    assert _cp(lib, q8, k2, v2, out8, lse8, n=4, layout=1 | (4 << 8)) == E_LAYOUT   # 2 KV heads, 4 groups
+    assert _cp(lib, q8, k2, v2, out8, lse8, n=4, layout=3 | (2 << 8)) == E_LAYOUT   # Ulysses takes no degree
 
 
 def test_attn_partial_and_merge_argument_errors(lib):

@@ -541,3 +541,24 @@ def test_head_grouped_tile_order_with_one_query_head_per_kv_head():
     ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, rows=rows)
     rt = torch.from_numpy(rows).cuda()
     compare(fo[rt].float().cpu(), fl[:, rt].cpu(), ro, rl, "head-grouped tile order")
+
+
+@pytest.mark.parametrize("layout,n,u,window,sizes,dims", [
+    ("zigzag", 4, 2, 0, None, (8, 4, 64, 64)), ("zigzag", 8, 4, 100, None, (8, 4, 64, 64)),
+    ("contiguous", 4, 4, 0, None, (8, 4, 64, 64)), ("chunked", 3, 2, 0, [700, 1, 1347], (8, 4, 64, 64)),
+    ("chunked", 2, 2, 0, [1000, 1048], (4, 4, 192, 128))])
+def test_cp_prefill_ulysses_ring_equals_the_ring(layout, n, u, window, sizes, dims):
+    """Ulysses x Ring (the layout word's degree u): each step's partial is computed as u head-group
+    items writing the same planes, so the result is bit-identical to the plain ring (or chunks) and
+    matches the oracle."""
+    S = 2048
+    Hq, Hkv, dqk, dv = dims
+    q, k, v = qkv(S, Hq, Hkv, dqk, dv, seed=91 + u + n, scale_v=0.7)
+    bo, bl = slope.cp_prefill(q, k, v, n, layout, chunk_sizes=sizes, window=window, out_dtype=torch.float32)
+    o, l = slope.cp_prefill(q, k, v, n, slope.layout_code(layout, u), chunk_sizes=sizes, window=window,
+                            out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert slope.device_status() == (0, 0)
+    assert torch.equal(o, bo) and torch.equal(l, bl)
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, window=window)
+    compare(o.cpu(), l.cpu(), ro, rl, f"ulysses x ring {layout} n={n} u={u} W={window}")

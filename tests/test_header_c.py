@@ -26,6 +26,10 @@ int main(void) {
          SLOPE_LAYOUT_ULYSSES);
   printf("dtypes %d %d\n", SLOPE_BF16, SLOPE_F32);
   printf("flags %u\n", SLOPE_CP_BF16_PARTIALS);
+  {
+    slope_layout l = (slope_layout)(SLOPE_LAYOUT_ZIGZAG | SLOPE_ULYSSES_DEGREE(4));
+    printf("layout_word %d\n", (int)l);
+  }
   return 0;
 }
 """
@@ -50,3 +54,4 @@ def test_header_compiles_as_c99_and_matches_the_binding(tmp_path):
     assert got["layouts"] == [slope.LAYOUTS[k] for k in ("contiguous", "zigzag", "chunked", "ulysses")]
     assert got["dtypes"] == [0, 1]
     assert got["flags"] == [slope.CP_BF16_PARTIALS]
+    assert got["layout_word"] == [slope.layout_code("zigzag", 4)]

@@ -140,3 +140,37 @@ def test_ulysses_plan_errors():
     for N in (0, 33):
         with pytest.raises(slope.SlopeError):
             slope.cp_prefill_plan(256, N, "ulysses")
+
+
+@pytest.mark.parametrize("layout,N,u,sizes", [("zigzag", 4, 2, None), ("contiguous", 8, 8, None),
+                                              ("chunked", 3, 4, [50, 1, 141]), ("zigzag", 1, 32, None)])
+@pytest.mark.parametrize("window", [0, 37])
+def test_ulysses_ring_plan_splits_each_item_by_head_group(layout, N, u, sizes, window):
+    """Ulysses x Ring: every base item becomes u head-group items of the same launch and plane; together
+    they cover every (head, visible pair) once."""
+    S = 192 if sizes is None else sum(sizes)
+    Hq = 64
+    base, nl0, np0 = slope.cp_prefill_plan(S, N, layout, chunk_sizes=sizes, window=window)
+    items, nl, npl = slope.cp_prefill_plan(S, N, slope.layout_code(layout, u), chunk_sizes=sizes, window=window)
+    assert (nl, npl) == (nl0, np0) and len(items) == u * len(base)
+    for i, it in enumerate(items):
+        b = base[i // u]
+        assert it["head_group"] == i % u and it["n_head_groups"] == u
+        assert {k: it[k] for k in ("launch", "plane", "q_row0", "q_len", "kv")} == \
+            {k: b[k] for k in ("launch", "plane", "q_row0", "q_len", "kv")}
+    vis = visible(S, window)
+    cnt = np.zeros((Hq, S, S), dtype=np.int32)
+    for it in items:
+        h0, h1 = it["head_group"] * Hq // u, (it["head_group"] + 1) * Hq // u
+        c, _ = coverage([it], S, window)
+        cnt[h0:h1] += c
+    assert np.array_equal(cnt, np.broadcast_to(vis.astype(np.int32), cnt.shape))
+
+
+def test_ulysses_ring_plan_errors():
+    with pytest.raises(slope.SlopeError):
+        slope.cp_prefill_plan(256, 4, slope.layout_code("ulysses", 2))   # Ulysses takes no extra degree
+    with pytest.raises(slope.SlopeError):
+        slope.cp_prefill_plan(256, 4, slope.layout_code("zigzag", 33))   # more than 32 groups
+    with pytest.raises(slope.SlopeError):
+        slope.cp_prefill_plan(256, 4, 1 | (1 << 16))                      # bits above the degree
