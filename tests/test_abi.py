@@ -150,6 +150,25 @@ def test_cp_prefill_ex_flags(lib):
     assert call(0, ws_bytes=w1) == E_WS  # fp32 partials need the larger workspace
 
 
+def test_empty_inputs_are_no_ops(lib):
+    """Zero query rows (attention) or zero rows (merge) return SLOPE_OK before any launch: no GPU is
+    touched here, and the descriptors may carry NULL data (strides as torch gives them for empty tensors)."""
+    Hq, Hkv, d = 4, 2, 64
+    q = _t([0, Hq, d], data=0)
+    k, v = _t([128, Hkv, d]), _t([128, Hkv, d])
+    out, lse = _t([0, Hq, d], dtype=1, data=0), _t([Hq, 0], dtype=1, data=0, stride=[1, 1])
+    assert lib.slope_attn_partial(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 0, 0, 1, 0, 0.0,
+                                  ctypes.byref(out), ctypes.byref(lse), None) == S_OK
+    o = (slope.SlopeTensor * 2)(_t([0, Hq, d], dtype=1, data=0), _t([0, Hq, d], dtype=0, data=0))
+    l = (slope.SlopeTensor * 2)(_t([Hq, 0], dtype=1, data=0, stride=[1, 1]), _t([Hq, 0], dtype=1, data=0, stride=[1, 1]))
+    fin = _t([0, Hq, d], dtype=0, data=0)
+    assert lib.slope_lse_merge(o, l, 2, ctypes.byref(fin), None, None) == E_DTYPE  # mixed partial dtypes
+    o = (slope.SlopeTensor * 2)(_t([0, Hq, d], dtype=0, data=0), _t([0, Hq, d], dtype=0, data=0))
+    assert lib.slope_lse_merge(o, l, 2, ctypes.byref(fin), None, None) == S_OK
+    assert _cp(lib, _t([0, Hq, d], data=0), _t([0, Hkv, d], data=0), _t([0, Hkv, d], data=0),
+               _t([0, Hq, d], data=0), _t([Hq, 0], dtype=1, data=0, stride=[1, 1])) == E_SHAPE  # a prefill needs tokens
+
+
 def test_workspace_size(lib):
     # ring: N planes of fp32 [S, Hq, dv] + lse; chunked: 2 planes
     ws = slope.cp_prefill_workspace_size(1024, 4, 64, 4, "zigzag")
