@@ -24,7 +24,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -68,18 +67,21 @@ def k1_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload_name):
-    """DRAM bytes per attention launch from the committed ncu summary, if it is for this kernel source."""
-    path = os.path.join(ROOT, "profiles", f"attn_partial_{workload_name}.md")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_partial_traffic.json")
+
+
+def profiled_traffic(workload_name, window=0):
+    """DRAM bytes per attention launch from the committed ncu record (profiles/attn_partial_traffic.json),
+    if that record was taken on the current kernel source; else None."""
     try:
-        text = open(path).read()
-    except OSError:
+        with open(TRAFFIC_FILE) as f:
+            records = json.load(f)
+    except (OSError, ValueError):
         return None
-    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_tr or m_hash.group(1) != k1_source_hash():
+    rec = records.get(f"{workload_name}/w{window}")
+    if not rec or rec.get("kernel_source_sha256_16") != k1_source_hash():
         return None
-    return float(m_tr.group(1))
+    return float(rec["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -222,6 +224,160 @@ def run_reference(args, w):
 
 # ---------------------------------------------------------------- GPU leg
 
+# The other full-size configurations, timed in the same default run after the headline workload
+# (each with its own clock record): the 64K chunked prefill, the 100K zigzag ring in full causal and
+# sliding-window-128 form, and the MLA-shaped chunked prefill.
+EXTRA_CONFIGS = [("chunked_prefill_s64k_c12k", 0), ("long_s100k_zigzag16_full_and_w128", 0),
+                 ("long_s100k_zigzag16_full_and_w128", 128), ("mla_s64k_d192_192_128_chunked_var", 0)]
+EXTRA_TIME_TARGET_MS = 1500.0  # timed work per extra configuration
+
+
+class Ctx:
+    """What every measurement of one bench run shares."""
+
+    def __init__(self, torch, slope, dist, local, peaks, peak_src, args):
+        self.torch, self.slope, self.dist, self.local = torch, slope, dist, local
+        self.peaks, self.peak_src, self.args = peaks, peak_src, args
+        self.world = dist.get_world_size() if dist is not None else 1
+        self.stream = torch.cuda.current_stream()
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+
+def k1_roofline(ctx, w, window, flops_step, steps, k1_ms, k1_n, k1_bytes, clocks):
+    """The attention kernel against its roof: the measured burst bf16 peak under a full causal mask (the
+    kernel is timed in launches of milliseconds, inside short steps at the sampled clock); the measured HBM
+    copy rate with a sliding window, where each tile sees a few key tiles only."""
+    peaks = ctx.peaks
+    k1_tflops = flops_step * steps / (k1_ms * 1e-3) / 1e12
+    k1_gbs = k1_bytes * k1_n / (k1_ms * 1e-3) / 1e9
+    common = {"traffic": profiled_traffic(w.name, window), "kernel": "attn_partial_kernel", "launches": k1_n,
+              "avg_launch_ms": k1_ms / max(1, k1_n), "bytes_per_launch": k1_bytes,
+              # one exponential per visible (query, key) pair and query head
+              "exp_per_s": flops_step / (2.0 * (w.dqk + w.dv)) * steps / (k1_ms * 1e-3),
+              "sm_mhz": clocks.get("sm_mhz")}
+    if window == 0:
+        r = {"bound": "tensor", "achieved": k1_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+             "frac": k1_tflops / peaks["bf16_tflops"], "peak_source": f"{ctx.peak_src} bf16_tflops (burst)",
+             "achieved_gbs": k1_gbs, **common}
+        mhz, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+        if mhz and mx:
+            # note only: the burst peak was measured at the maximum clock
+            r["frac_of_peak_at_sampled_clock"] = k1_tflops / (peaks["bf16_tflops"] * mhz / mx)
+        return r
+    return {"bound": "hbm", "achieved": k1_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": k1_gbs / peaks["hbm_gbs"], "peak_source": f"{ctx.peak_src} hbm_gbs",
+            "achieved_tflops": k1_tflops, **common}
+
+
+def measure_job(ctx, w, window, q, k, v, steps, warmup, flags=()):
+    """Times `steps` whole slope_cp_prefill calls (all attention launches + the merge) after `warmup`
+    untimed ones, with CUDA events around every launch on the launching stream and the clocks sampled
+    during the timed region.  Returns the measured record."""
+    torch, slope = ctx.torch, ctx.slope
+    sizes = wl.chunk_sizes(w)
+    n = wl.n_chunks(w)
+    out = torch.empty((w.S, w.Hq, w.dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.Hq, w.S), dtype=torch.float32, device="cuda")
+    ws = torch.empty((slope.cp_prefill_workspace_size(w.S, w.Hq, w.dv, n, w.layout, sizes),), dtype=torch.uint8,
+                     device="cuda")
+    stream = ctx.stream
+
+    def step():
+        slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window, out=out, lse=lse, workspace=ws)
+
+    _, launches_per_step, _ = slope.cp_prefill_plan(w.S, n, w.layout, chunk_sizes=sizes, window=window)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    st, site = slope.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} at site {site}")
+
+    n_pairs = launches_per_step + 8
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_pairs)]
+          for _ in range(steps)]
+    for step_ev in ev:
+        for a, b in step_ev:  # materialise the CUDA events
+            a.record(stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(ctx.local)
+    sampler.start()
+    time.sleep(0.15)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kinds_all, counts = [], []
+    ctx.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for s in range(steps):
+        _, _, nl, kinds = slope.cp_prefill_timed(q, k, v, n, w.layout, ev[s], chunk_sizes=sizes, window=window,
+                                                 out=out, lse=lse, workspace=ws)
+        counts.append(nl)
+        kinds_all.append(kinds)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    ctx.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), ctx.dist, "cuda")
+    st, site = slope.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} at site {site}")
+
+    k1_ms, k2_ms, k1_n, k2_n = 0.0, 0.0, 0, 0
+    for s in range(steps):
+        for i in range(counts[s]):
+            a, b = ev[s][i]
+            d = a.elapsed_time(b)
+            if kinds_all[s][i] == 0:
+                k1_ms += d
+                k1_n += 1
+            else:
+                k2_ms += d
+                k2_n += 1
+    flops_step = workload_flops(w, window)
+    merge_bytes = merge_bytes_per_launch(slope, w, n, sizes, window)
+    k2_gbs = merge_bytes * k2_n / (k2_ms * 1e-3) / 1e9 if k2_ms > 0 else None
+    k1_bytes, k1_launches_per_step = k1_bytes_per_launch(slope, w, n, sizes, window)
+    if k1_n != k1_launches_per_step * steps:
+        raise RuntimeError(f"attention launches {k1_n} != {k1_launches_per_step} per step x {steps}")
+    peaks = ctx.peaks
+    rec = {
+        "value": job_tflops(flops_step, steps, ctx.world, elapsed_ms), "unit": UNIT,
+        "ms_per_step": elapsed_ms / steps, "steps": steps, "warmup": warmup,
+        "tokens_per_s": w.S * steps * ctx.world / (elapsed_ms * 1e-3),
+        "roofline": k1_roofline(ctx, w, window, flops_step, steps, k1_ms, k1_n, k1_bytes, clocks),
+        "roofline_merge": {"bound": "hbm", "achieved": k2_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": (k2_gbs / peaks["hbm_gbs"]) if k2_gbs else None,
+                           "peak_source": f"{ctx.peak_src} hbm_gbs",
+                           "bytes_per_launch": merge_bytes, "kernel": "lse_merge_kernel",
+                           "avg_launch_ms": k2_ms / max(1, k2_n)},
+        "gpu_launches": int(sum(counts)),
+        "clocks": clocks,
+        "config": {"workload": w.name, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "dqk": w.dqk, "dv": w.dv,
+                   "layout": w.layout, "n_chunks": n, "window": window, "batch": 1,
+                   "l2": f"inputs larger than L2 (Q+K+V {q.numel() * 2 + k.numel() * 2 + v.numel() * 2} B, "
+                         f"partials {ws.numel()} B > {L2_BYTES} B); no flush",
+                   "flops_per_step": flops_step},
+    }
+    return rec, ws
+
+
+def steps_for(ctx, step, target_ms, max_steps, warmup):
+    """Number of timed steps that fill about target_ms (at least 3), from the warm-up steps' time."""
+    torch = ctx.torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(ctx.stream)
+    for _ in range(warmup):
+        step()
+    b.record(ctx.stream)
+    torch.cuda.synchronize()
+    per = a.elapsed_time(b) / max(1, warmup)
+    return int(max(3, min(max_steps, round(target_ms / max(per, 1e-3)))))
+
+
 def run_gpu(args, w):
     import torch
 
@@ -236,145 +392,65 @@ def run_gpu(args, w):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
     slope.build()
     slope.load()
+    peaks, peak_src = load_peaks()
+    ctx = Ctx(torch, slope, dist, local, peaks, peak_src, args)
     window = args.window
     q, k, v = wl.workload_qkv(w, device="cuda")
     sizes = wl.chunk_sizes(w)
     n = wl.n_chunks(w)
+
+    head, ws = measure_job(ctx, w, window, q, k, v, args.steps, args.warmup)
     out = torch.empty((w.S, w.Hq, w.dv), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((w.Hq, w.S), dtype=torch.float32, device="cuda")
-    ws = torch.empty((slope.cp_prefill_workspace_size(w.S, w.Hq, w.dv, n, w.layout, sizes),), dtype=torch.uint8,
-                     device="cuda")
-    stream = torch.cuda.current_stream()
-
-    def step():
-        slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window, out=out, lse=lse, workspace=ws)
-
-    _, launches_per_step, _ = slope.cp_prefill_plan(w.S, n, w.layout, chunk_sizes=sizes, window=window)
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    st, site = slope.device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} at site {site}")
-
-    # ---- timed region: K steps, per-launch events on the launching stream
-    n_pairs = launches_per_step + 8
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_pairs)]
-          for _ in range(args.steps)]
-    for step_ev in ev:
-        for a, b in step_ev:  # materialise the CUDA events
-            a.record(stream)
-            b.record(stream)
-    torch.cuda.synchronize()
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.15)
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    kinds_all, counts = [], []
-    barrier()
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    for s in range(args.steps):
-        _, _, nl, kinds = slope.cp_prefill_timed(q, k, v, n, w.layout, ev[s], chunk_sizes=sizes, window=window,
-                                                 out=out, lse=lse, workspace=ws)
-        counts.append(nl)
-        kinds_all.append(kinds)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    clocks = sampler.stop()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, "cuda")
-    st, site = slope.device_status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} at site {site}")
-
-    k1_ms, k2_ms, k1_n, k2_n = 0.0, 0.0, 0, 0
-    for s in range(args.steps):
-        for i in range(counts[s]):
-            a, b = ev[s][i]
-            d = a.elapsed_time(b)
-            if kinds_all[s][i] == 0:
-                k1_ms += d
-                k1_n += 1
-            else:
-                k2_ms += d
-                k2_n += 1
-
-    flops_step = workload_flops(w, window)
-    value = job_tflops(flops_step, args.steps, world, elapsed_ms)
-    tokens_s = w.S * args.steps * world / (elapsed_ms * 1e-3)
-    peaks, peak_src = load_peaks()
-    k1_tflops = flops_step * args.steps / (k1_ms * 1e-3) / 1e12
-    merge_bytes = merge_bytes_per_launch(slope, w, n, sizes, window)
-    k2_gbs = merge_bytes * k2_n / (k2_ms * 1e-3) / 1e9 if k2_ms > 0 else None
-
-    # ---- the attention kernel's roofline: tensor-bound under a full causal mask; with a sliding
-    # window each tile sees a few key tiles only and the kernel is measured against HBM
-    k1_bytes, k1_launches_per_step = k1_bytes_per_launch(slope, w, n, sizes, window)
-    k1_gbs = k1_bytes * k1_n / (k1_ms * 1e-3) / 1e9
-    k1_common = {"traffic": profiled_traffic(w.name) if window == 0 else None, "kernel": "attn_partial_kernel",
-                 "launches": k1_n, "avg_launch_ms": k1_ms / max(1, k1_n), "bytes_per_launch": k1_bytes,
-                 # one exponential per visible (query, key) pair and query head
-                 "exp_per_s": flops_step / (2.0 * (w.dqk + w.dv)) * args.steps / (k1_ms * 1e-3)}
-    if k1_n != k1_launches_per_step * args.steps:
-        raise RuntimeError(f"attention launches {k1_n} != {k1_launches_per_step} per step x {args.steps}")
-    if window == 0:
-        k1_roofline = {"bound": "tensor", "achieved": k1_tflops, "peak": peaks["bf16_tflops_sustained"],
-                       "unit": "TFLOP/s", "frac": k1_tflops / peaks["bf16_tflops_sustained"],
-                       "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a multi-launch step)",
-                       "achieved_gbs": k1_gbs, **k1_common}
-    else:
-        k1_roofline = {"bound": "hbm", "achieved": k1_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                       "frac": k1_gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} hbm_gbs",
-                       "achieved_tflops": k1_tflops, **k1_common}
-
-    # ---- the same attention as one launch (bf16 out, no partials, no merge): the fused single-GPU form
-    fused = None if args.no_variants else run_fused(slope, torch, w, window, q, k, v, stream, args, barrier, dist)
-
-    # ---- the same step with the partials kept in bf16 between the attention launches and the merge
-    bf16p = None
+    stream = ctx.stream
+    variants = {}
     if not args.no_variants:
-        bf16p = run_bf16_partials(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream, args, barrier, dist)
-        bf16p["gpu_launches_per_step"] = counts[0]  # the same launches as the fp32-partial step
-
-    # ---- the same attention in the head-sharded (Ulysses) layout
-    ulysses = None if args.no_variants else run_ulysses(slope, torch, w, window, q, k, v, out, lse, stream, args,
-                                                         barrier, dist)
-
-    # ---- end to end through the public call with pinned host buffers
-    e2e = None if args.no_e2e else run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrier,
-                                           dist)
+        # the same attention as one launch (bf16 out, no partials, no merge): the fused single-GPU form
+        variants["fused_single_launch"] = run_fused(slope, torch, w, window, q, k, v, stream, args, ctx.barrier,
+                                                    dist)
+        # the ring / chunked layout with each rank's queries run over all their visible keys in one item
+        variants["fused_layout"] = run_fused_layout(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream,
+                                                    args, ctx.barrier, dist)
+        # the same step with the partials kept in bf16 between the attention launches and the merge
+        variants["bf16_partials"] = run_bf16_partials(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream,
+                                                      args, ctx.barrier, dist)
+        variants["bf16_partials"]["gpu_launches_per_step"] = head["gpu_launches"] // args.steps
+        # the same attention in the head-sharded (Ulysses) layout
+        variants["ulysses"] = run_ulysses(slope, torch, w, window, q, k, v, out, lse, stream, args, ctx.barrier,
+                                          dist)
+    # end to end through the public call with pinned host buffers
+    e2e = None if args.no_e2e else run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args,
+                                           ctx.barrier, dist)
+    del q, k, v, ws, out, lse
+    torch.cuda.empty_cache()
 
     result = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "dqk": w.dqk, "dv": w.dv,
-                   "layout": w.layout, "n_chunks": n, "window": window, "batch": 1,
-                   "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": f"inputs larger than L2 (Q+K+V {q.numel() * 2 + k.numel() * 2 + v.numel() * 2} B, "
-                         f"partials {ws.numel()} B > {L2_BYTES} B); no flush",
-                   "flops_per_step": flops_step},
-        "tokens_per_s": tokens_s,
-        "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],
-        "roofline": k1_roofline,
-        "roofline_merge": {"bound": "hbm", "achieved": k2_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                           "frac": (k2_gbs / peaks["hbm_gbs"]) if k2_gbs else None,
-                           "bytes_per_launch": merge_bytes, "kernel": "lse_merge_kernel",
-                           "avg_launch_ms": k2_ms / max(1, k2_n)},
+        "config": {**head["config"], "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "tokens_per_s": head["tokens_per_s"],
+        "pct_of_bf16_peak": 100.0 * head["value"] / world / peaks["bf16_tflops"],
+        "roofline": head["roofline"],
+        "roofline_merge": head["roofline_merge"],
         "e2e": e2e,
-        "fused_single_launch": fused,
-        "bf16_partials": bf16p,
-        "ulysses": ulysses,
-        "gpu_launches": int(sum(counts)),
-        "clocks": clocks,
+        **variants,
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
     }
+
+    # ---- the other full-size configurations, each with its own clock record
+    if not args.only_workload:
+        configs = {}
+        for name, win in EXTRA_CONFIGS:
+            wx = wl.BY_NAME[name]
+            configs[f"{name}/w{win}"] = run_extra(ctx, wx, win, args)
+            torch.cuda.empty_cache()
+        result["configs"] = configs
+        result["gate"] = gate_summary(result)
+
     if rank == 0 and not args.no_cpu_baseline:
         v_cpu, dt, desc, cores = oracle_sample(w, args.cpu_seconds)
         result["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
@@ -384,6 +460,45 @@ def run_gpu(args, w):
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def run_extra(ctx, w, window, args):
+    """One more full-size configuration: the whole job (attention launches + merge) with its attention and
+    merge rooflines, its fused-layout form and, for the MLA-shaped workload, the host-buffer end to end."""
+    torch, slope = ctx.torch, ctx.slope
+    q, k, v = wl.workload_qkv(w, device="cuda")
+    sizes = wl.chunk_sizes(w)
+    n = wl.n_chunks(w)
+    out = torch.empty((w.S, w.Hq, w.dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.Hq, w.S), dtype=torch.float32, device="cuda")
+    ws0 = torch.empty((slope.cp_prefill_workspace_size(w.S, w.Hq, w.dv, n, w.layout, sizes),), dtype=torch.uint8,
+                      device="cuda")
+
+    def step():
+        slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window, out=out, lse=lse, workspace=ws0)
+
+    steps = steps_for(ctx, step, EXTRA_TIME_TARGET_MS, args.steps, args.warmup)
+    del ws0
+    rec, ws = measure_job(ctx, w, window, q, k, v, steps, args.warmup)
+    sub = argparse.Namespace(**{**vars(args), "steps": steps})
+    if not args.no_variants:
+        rec["fused_layout"] = run_fused_layout(slope, torch, w, n, sizes, window, q, k, v, out, lse, ctx.stream, sub,
+                                               ctx.barrier, ctx.dist)
+    if not args.no_e2e and w.dqk != w.dv:
+        rec["e2e"] = run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, ctx.stream,
+                             argparse.Namespace(**{**vars(args), "steps": max(steps, 10)}), ctx.barrier, ctx.dist)
+    del q, k, v, out, lse, ws
+    return rec
+
+
+def gate_summary(result):
+    """Each configuration's attention-kernel fraction and merge fraction of its measured roof."""
+    rows = {f"{result['config']['workload']}/w{result['config']['window']}": result}
+    rows.update(result.get("configs", {}))
+    return {key: {"k1_frac": r["roofline"]["frac"], "k1_bound": r["roofline"]["bound"],
+                  "merge_frac": r["roofline_merge"]["frac"], "job_tflops": r["value"],
+                  "sm_mhz": r["clocks"].get("sm_mhz"), "reasons": r["clocks"].get("reasons")}
+            for key, r in rows.items()}
 
 
 def merge_bytes_per_launch(slope, w, n, sizes, window):
@@ -482,6 +597,23 @@ def run_fused(slope, torch, w, window, q, k, v, stream, args, barrier, dist):
     return {"value": job_tflops(workload_flops(w, window), args.steps, world, ms), "unit": UNIT,
             "ms_per_step": ms / args.steps, "api": "slope_attn_partial over the whole sequence, bf16 out",
             "gpu_launches_per_step": 1}
+
+
+def run_fused_layout(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream, args, barrier, dist):
+    """The workload's own layout with SLOPE_CP_FUSED: every rank's (or chunk's) query rows attend to all of
+    their visible keys in one work item, merged online in the kernel (no partial planes, no merge launch)."""
+    nbytes = slope.cp_prefill_workspace_size(w.S, w.Hq, w.dv, n, w.layout, sizes, fused=True)
+    wsf = torch.empty((max(nbytes, 256),), dtype=torch.uint8, device="cuda")
+
+    def step():
+        slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window, out=out, lse=lse, workspace=wsf,
+                         fused=True)
+
+    ms, world = time_variant(torch, step, stream, args, barrier, dist)
+    _, n_launch, _ = slope.cp_prefill_plan(w.S, n, w.layout, chunk_sizes=sizes, window=window, fused=True)
+    return {"value": job_tflops(workload_flops(w, window), args.steps, world, ms), "unit": UNIT,
+            "ms_per_step": ms / args.steps, "api": "slope_cp_prefill_ex(SLOPE_CP_FUSED)",
+            "gpu_launches_per_step": n_launch}
 
 
 def time_variant(torch, step, stream, args, barrier, dist):
@@ -593,6 +725,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the fused, bf16-partial and Ulysses legs (profiling runs)")
+    ap.add_argument("--only-workload", action="store_true",
+                    help="time the chosen workload alone, not the other full-size configurations after it")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

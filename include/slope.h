@@ -24,8 +24,12 @@
  *    token-major (batch 1).  Row and head strides of Q/K/V must be multiples
  *    of 8 elements (16 bytes) and the data pointer 16-byte aligned, because
  *    the kernels read them with the Tensor Memory Accelerator.
- *  - Supported head sizes (dqk, dv): (64, 64), (128, 64), (128, 128) and
- *    (192, 128); other pairs return SLOPE_ERR_UNSUPPORTED.  Hq must be a
+ *  - Supported head sizes: dqk in {64, 128, 192} with dv in {64, 128}; other
+ *    pairs return SLOPE_ERR_UNSUPPORTED.  dv = 192 is refused because the
+ *    attention kernel keeps two 128-row query tiles per SM, each with a 128-
+ *    column score tile and a dv-column output accumulator in tensor memory:
+ *    2 x (128 + 192) = 640 columns, more than the 512 an SM has.  The merge
+ *    alone (slope_lse_merge) takes dv in {64, 128, 192}.  Hq must be a
  *    multiple of Hkv; query head h reads key/value head h / (Hq / Hkv).
  *  - Masks use GLOBAL token positions: key j is visible to query i iff
  *    (!causal || pos(j) <= pos(i)) && (window == 0 || pos(i) - pos(j) < window).
@@ -87,7 +91,10 @@ typedef enum {
   SLOPE_LAYOUT_CONTIGUOUS = 0, /* ring of n ranks, rank r owns tokens [r*S/n, (r+1)*S/n)          */
   SLOPE_LAYOUT_ZIGZAG = 1,     /* ring of n ranks, rank r owns sub-chunks r and 2n-1-r of S/(2n)  */
   SLOPE_LAYOUT_CHUNKED = 2,    /* chunked prefill: chunk c attends to all earlier tokens + itself */
-  SLOPE_LAYOUT_ULYSSES = 3     /* n ranks, rank u owns every token of query-head group u of n     */
+  SLOPE_LAYOUT_ULYSSES = 3,    /* n ranks, rank u owns every token of query-head group u of n     */
+  /* Not a layout: widens the enum's range to 16 bits, so that a layout word carrying a Ulysses
+   * degree (SLOPE_ULYSSES_DEGREE below) is a valid value of this type in C++ as well as in C. */
+  SLOPE_LAYOUT_WORD_MAX_ = 0xffff
 } slope_layout;
 
 /*
@@ -110,6 +117,10 @@ typedef enum {
  *
  *   q   bf16 [Sq, Hq, dqk]    k bf16 [Skv, Hkv, dqk]    v bf16 [Skv, Hkv, dv]
  *   q_off / kv_off: global positions of q row 0 / k row 0 (the masks use them).
+ *       Every position must lie in [-2^28, 2^28]: q_off >= -2^28, q_off + Sq <= 2^28,
+ *       and the same for kv_off and Skv (else SLOPE_ERR_SHAPE), because the kernel
+ *       takes differences of a query and a key position, less the window, in 32-bit
+ *       integers.
  *   causal, window, scale: see the conventions above.
  *   out fp32 or bf16 [Sq, Hq, dv]: the softmax-normalised output over the
  *       visible keys of this block (0 for rows that see none).  Innermost
@@ -133,7 +144,7 @@ SLOPE_API slope_status slope_attn_partial(const slope_tensor* q, const slope_ten
  *   L   = log sum_k exp(lse_k)            (max-shifted; all -inf gives -inf)
  *   out = sum_k exp(lse_k - L) * out_k     (partials with lse_k = -inf are skipped)
  *
- *   outs[k] fp32 or bf16 [S, H, dv], all of one dtype (else SLOPE_ERR_DTYPE);
+ *   outs[k] fp32 or bf16 [S, H, dv], dv in {64, 128, 192}, all of one dtype (else SLOPE_ERR_DTYPE);
  *        lses[k] fp32 rank 2 [H, S] (any strides), 1 <= n <= 32.  bf16 partials
  *        are widened to fp32 as they are read; the sums run in fp32 either way.
  *   out: bf16 or fp32 [S, H, dv] (innermost stride 1, row/head strides multiples
@@ -206,7 +217,12 @@ SLOPE_API slope_status slope_cp_prefill(const slope_tensor* q, const slope_tenso
  *
  * The first call on a device looks up the scratch array's device address
  * (with that device current) and keeps it; make that first call before any
- * stream capture.  Every call on a device shares the one array and it keeps
+ * stream capture.  The 64 MiB are committed on a device when the library's
+ * module is loaded there; with CUDA's lazy module loading (the default since
+ * CUDA 12.2) that happens at that first call.  A caller that reserves the rest
+ * of the device memory for its own pools should therefore make the first call
+ * before reserving them, or the first call may fail with SLOPE_ERR_CUDA (out of
+ * memory).  Every call on a device shares the one array and it keeps
  * the last call's contents (nothing in it needs to start at zero: each call
  * writes every partial the merge reads).  Calls whose work overlaps on the
  * GPU (for example on two streams) race on the array and give wrong results;
@@ -223,7 +239,8 @@ SLOPE_API size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t 
                                        const int64_t* chunk_sizes);
 
 /* Flags of slope_cp_prefill_ex. */
-#define SLOPE_CP_BF16_PARTIALS 1u /* keep the partial outputs in bf16 (lse stays fp32) */
+#define SLOPE_CP_BF16_PARTIALS 1u /* keep the partial outputs in bf16 (lse stays fp32)            */
+#define SLOPE_CP_FUSED 2u         /* merge each rank's / chunk's partials online, in the kernel    */
 
 /*
  * slope_cp_prefill with options.  flags = 0 is slope_cp_prefill exactly.
@@ -238,6 +255,25 @@ SLOPE_API size_t slope_cp_prefill_workspace_size(int64_t S, int64_t Hq, int64_t 
  * positive and sum to 1, rounding each partial once more moves the final
  * output by at most one bf16 rounding (relative 2^-8) of the largest partial
  * element, before the output's own rounding when out is bf16.
+ *
+ * SLOPE_CP_FUSED: the ring and chunked layouts without partial planes and
+ * without the merge launch.  Over a whole ring, each query sub-chunk of rank r
+ * meets every key/value block once (Moreh, section "Introduction to Context
+ * Parallelism", Ring Attention item: the blocks circulate until every device
+ * has seen all of them), so its partials cover disjoint key sets whose union
+ * is every key; under the masks that union is one contiguous key range.  With
+ * this flag each query sub-chunk (ZIGZAG: two per rank; CONTIGUOUS: one) or
+ * chunk (CHUNKED: its prefix and its diagonal) is one work item whose online
+ * softmax runs over that range, key tiles in ascending order, and writes out
+ * and lse directly: the same attention as the partials and the exact merge,
+ * up to the order in which fp32 sums are taken.  The items of all ranks (or
+ * chunks) share attention launches up to 32 items each.  A Ulysses degree in
+ * the layout word still splits every item by head group.  SLOPE_LAYOUT_ULYSSES
+ * already writes out directly; the flag changes nothing there.  A bf16 out
+ * needs row/head strides that are multiples of 8 elements and a 16-byte
+ * aligned pointer.  The workspace then holds only an lse plane (used when lse
+ * is NULL).  Together with SLOPE_CP_BF16_PARTIALS (no partials to keep)
+ * the call returns SLOPE_ERR_UNSUPPORTED.
  *
  * Unknown flag bits return SLOPE_ERR_UNSUPPORTED.  The workspace must hold
  * slope_cp_prefill_workspace_size_ex(..., flags) bytes (the flags = 0 size is
@@ -335,6 +371,16 @@ typedef struct {
 SLOPE_API int64_t slope_cp_prefill_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes,
                               int causal, int64_t window, slope_plan_item* items, int64_t capacity,
                               int32_t* n_launches, int32_t* n_planes);
+
+/*
+ * slope_cp_prefill_plan for the decomposition slope_cp_prefill_ex performs with
+ * these flags (SLOPE_CP_FUSED: one item per query sub-chunk or chunk, each over
+ * its whole visible key range, one plane written directly).  Unknown or
+ * conflicting flags return SLOPE_ERR_UNSUPPORTED.
+ */
+SLOPE_API int64_t slope_cp_prefill_plan_ex(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes,
+                                           int causal, int64_t window, unsigned flags, slope_plan_item* items,
+                                           int64_t capacity, int32_t* n_launches, int32_t* n_planes);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of the

@@ -57,10 +57,11 @@ EXPORTED = ["slope_attn_partial", "slope_lse_merge", "slope_cp_prefill", "slope_
             "slope_cp_prefill_timed", "slope_cp_prefill_plan", "slope_device_status",
             "slope_debug_timeout_selftest", "slope_status_string", "slope_version", "slope_last_error",
             "slope_cp_prefill_static_scratch", "slope_cp_prefill_host", "slope_cp_prefill_ex",
-            "slope_cp_prefill_workspace_size_ex"]
+            "slope_cp_prefill_workspace_size_ex", "slope_cp_prefill_plan_ex"]
 
 # flags of slope_cp_prefill_ex (include/slope.h)
 CP_BF16_PARTIALS = 1
+CP_FUSED = 2
 
 
 def build(force: bool = False) -> str:
@@ -94,6 +95,9 @@ def load():
     lib.slope_cp_prefill_plan.argtypes = [i64, c_int, c_int, P(i64), c_int, i64, P(SlopePlanItem), i64,
                                           P(ctypes.c_int32), P(ctypes.c_int32)]
     lib.slope_cp_prefill_plan.restype = i64
+    lib.slope_cp_prefill_plan_ex.argtypes = [i64, c_int, c_int, P(i64), c_int, i64, ctypes.c_uint, P(SlopePlanItem),
+                                             i64, P(ctypes.c_int32), P(ctypes.c_int32)]
+    lib.slope_cp_prefill_plan_ex.restype = i64
     lib.slope_device_status.argtypes = [vp, P(c_int)]
     lib.slope_device_status.restype = c_int
     lib.slope_debug_timeout_selftest.argtypes = [ctypes.c_uint64, vp]
@@ -233,15 +237,22 @@ def lse_merge(outs, lses, *, out=None, lse=None, out_dtype=None, stream=None):
     return out, lse
 
 
-def cp_prefill_workspace_size(S, Hq, dv, n_chunks, layout, chunk_sizes=None, bf16_partials=False) -> int:
+def _flags(bf16_partials=False, fused=False):
+    return (CP_BF16_PARTIALS if bf16_partials else 0) | (CP_FUSED if fused else 0)
+
+
+def cp_prefill_workspace_size(S, Hq, dv, n_chunks, layout, chunk_sizes=None, bf16_partials=False,
+                              fused=False) -> int:
     arr, ptr = _chunk_array(chunk_sizes)
-    if bf16_partials:
+    flags = _flags(bf16_partials, fused)
+    if flags:
         return int(load().slope_cp_prefill_workspace_size_ex(int(S), int(Hq), int(dv), int(n_chunks), _layout(layout),
-                                                             ptr, CP_BF16_PARTIALS))
+                                                             ptr, flags))
     return int(load().slope_cp_prefill_workspace_size(int(S), int(Hq), int(dv), int(n_chunks), _layout(layout), ptr))
 
 
-def _prep_cp(q, v, n_chunks, layout, chunk_sizes, out, lse, workspace, out_dtype, want_lse, bf16_partials=False):
+def _prep_cp(q, v, n_chunks, layout, chunk_sizes, out, lse, workspace, out_dtype, want_lse, bf16_partials=False,
+             fused=False):
     torch = _torch()
     S, Hq, _ = q.shape
     dv = v.shape[2]
@@ -250,7 +261,7 @@ def _prep_cp(q, v, n_chunks, layout, chunk_sizes, out, lse, workspace, out_dtype
     if lse is None and want_lse:
         lse = torch.empty((Hq, S), dtype=torch.float32, device=q.device)
     if workspace is None:
-        nbytes = cp_prefill_workspace_size(S, Hq, dv, n_chunks, layout, chunk_sizes, bf16_partials)
+        nbytes = cp_prefill_workspace_size(S, Hq, dv, n_chunks, layout, chunk_sizes, bf16_partials, fused)
         if nbytes == 0:
             raise SlopeError(-5, "slope_cp_prefill_workspace_size")
         workspace = torch.empty((nbytes,), dtype=torch.uint8, device=q.device)
@@ -258,15 +269,18 @@ def _prep_cp(q, v, n_chunks, layout, chunk_sizes, out, lse, workspace, out_dtype
 
 
 def cp_prefill(q, k, v, n_chunks, layout="zigzag", *, chunk_sizes=None, causal=True, window=0, scale=0.0,
-               out=None, lse=None, workspace=None, out_dtype=None, want_lse=True, stream=None, bf16_partials=False):
+               out=None, lse=None, workspace=None, out_dtype=None, want_lse=True, stream=None, bf16_partials=False,
+               fused=False):
     """Context-parallel prefill attention of one layer (ring steps or chunks run in order, then merged).
 
     Returns ``(out, lse)``: out bf16 (default) or fp32 [S,Hq,dv], lse fp32 [Hq,S] (None if not wanted).
     ``bf16_partials`` keeps the partial outputs in bf16 between the attention launches and the merge
-    (slope_cp_prefill_ex with SLOPE_CP_BF16_PARTIALS); otherwise slope_cp_prefill runs.
+    (SLOPE_CP_BF16_PARTIALS); ``fused`` merges each rank's or chunk's partials online in the kernel, with no
+    partial planes and no merge launch (SLOPE_CP_FUSED).  Either runs slope_cp_prefill_ex; otherwise
+    slope_cp_prefill runs.
     """
     out, lse, workspace = _prep_cp(q, v, n_chunks, layout, chunk_sizes, out, lse, workspace, out_dtype, want_lse,
-                                   bf16_partials)
+                                   bf16_partials, fused)
     arr, ptr = _chunk_array(chunk_sizes)
     dq, dk, dvv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     dl = _desc(lse) if lse is not None else None
@@ -274,8 +288,9 @@ def cp_prefill(q, k, v, n_chunks, layout="zigzag", *, chunk_sizes=None, causal=T
                  int(bool(causal)), int(window), float(scale))
     args_tail = (ctypes.byref(do), ctypes.byref(dl) if dl is not None else None,
                  ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
-    if bf16_partials:
-        st = load().slope_cp_prefill_ex(*args_head, CP_BF16_PARTIALS, *args_tail)
+    flags = _flags(bf16_partials, fused)
+    if flags:
+        st = load().slope_cp_prefill_ex(*args_head, flags, *args_tail)
         _check(st, "slope_cp_prefill_ex")
     else:
         st = load().slope_cp_prefill(*args_head, *args_tail)
@@ -367,18 +382,20 @@ def cp_prefill_timed(q, k, v, n_chunks, layout, events, *, chunk_sizes=None, cau
     return out, lse, nl.value, list(kinds)[:nl.value]
 
 
-def cp_prefill_plan(S, n_chunks, layout, *, chunk_sizes=None, causal=True, window=0):
-    """Host-only work decomposition: (items, n_launches, n_planes); items are dicts."""
+def cp_prefill_plan(S, n_chunks, layout, *, chunk_sizes=None, causal=True, window=0, fused=False):
+    """Host-only work decomposition: (items, n_launches, n_planes); items are dicts.  ``fused`` gives the
+    decomposition of SLOPE_CP_FUSED."""
     lib = load()
     arr, ptr = _chunk_array(chunk_sizes)
     nl, npl = ctypes.c_int32(0), ctypes.c_int32(0)
-    n = lib.slope_cp_prefill_plan(int(S), int(n_chunks), _layout(layout), ptr, int(bool(causal)), int(window),
-                                  None, 0, ctypes.byref(nl), ctypes.byref(npl))
+    flags = _flags(fused=fused)
+    n = lib.slope_cp_prefill_plan_ex(int(S), int(n_chunks), _layout(layout), ptr, int(bool(causal)), int(window),
+                                     flags, None, 0, ctypes.byref(nl), ctypes.byref(npl))
     if n < 0:
         raise SlopeError(int(n), "slope_cp_prefill_plan")
     items = (SlopePlanItem * max(1, n))()
-    n2 = lib.slope_cp_prefill_plan(int(S), int(n_chunks), _layout(layout), ptr, int(bool(causal)), int(window),
-                                   items, n, None, None)
+    n2 = lib.slope_cp_prefill_plan_ex(int(S), int(n_chunks), _layout(layout), ptr, int(bool(causal)), int(window),
+                                      flags, items, n, None, None)
     assert n2 == n
     res = []
     for it in items[:n]:

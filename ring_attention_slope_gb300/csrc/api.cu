@@ -21,6 +21,9 @@ namespace {
 
 constexpr int kMaxRanks = 32;
 constexpr int64_t kMaxSeq = int64_t(1) << 30;
+// Bound on the global positions slope_attn_partial accepts: the kernel forms differences of a query
+// and a key position, less the window, in 32-bit integers, which then stay within +-1.5 * 2^30.
+constexpr int64_t kMaxPos = int64_t(1) << 28;
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 
 // ---------------------------------------------------------------- argument checks
@@ -202,7 +205,7 @@ slope_status chunk_list(int64_t S, int n_chunks, const int64_t* chunk_sizes, std
 // all-to-all, rank u holds every token of head group u of N and computes the whole
 // attention of those heads: one item per rank, written as the final output.
 slope_status build_base_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
-                             int64_t window, Plan& plan) {
+                             int64_t window, bool fused, Plan& plan) {
   plan = Plan();
   if (S <= 0 || S > kMaxSeq) return SLOPE_ERR_SHAPE;
   if (window < 0) return SLOPE_ERR_SHAPE;
@@ -219,6 +222,30 @@ slope_status build_base_plan(int64_t S, int n_chunks, slope_layout layout, const
       out[1] = 2 * N - 1 - r;
       return 2;
     };
+    if (fused) {
+      // Every ring step of rank r visits one of the ranks' blocks, so over the whole ring each of
+      // r's query sub-chunks meets every key block once: their union is all S keys, of which the
+      // masks leave one range.  One item per sub-chunk runs its online softmax over that range and
+      // writes the final output.
+      for (int r = 0; r < N; ++r) {
+        int64_t qa[2];
+        const int nq = owned(r, qa);
+        for (int i = 0; i < nq; ++i) {
+          PItem it{};
+          it.launch = r;
+          it.plane = 0;
+          it.q_row0 = qa[i] * sub;
+          it.q_len = sub;
+          int64_t k0 = 0, k1 = S;
+          if (trim(it.q_row0, it.q_row0 + sub, k0, k1, causal, window)) it.kv[it.n_kv++] = Range{k0, k1 - k0};
+          plan.items.push_back(it);
+        }
+      }
+      plan.n_launches = N;
+      plan.n_planes = 1;
+      plan.direct = true;
+      return SLOPE_OK;
+    }
     for (int t = 0; t < N; ++t) {
       for (int r = 0; r < N; ++r) {
         const int src = ((r - t) % N + N) % N;
@@ -247,6 +274,26 @@ slope_status build_base_plan(int64_t S, int n_chunks, slope_layout layout, const
     std::vector<int64_t> sizes;
     slope_status st = chunk_list(S, n_chunks, chunk_sizes, sizes);
     if (st != SLOPE_OK) return st;
+    if (fused) {
+      // chunk [s, e): its prefix partial and its diagonal partial in one item over keys [0, e)
+      int64_t s0 = 0;
+      for (size_t c = 0; c < sizes.size(); ++c) {
+        const int64_t s1 = s0 + sizes[c];
+        PItem it{};
+        it.launch = static_cast<int>(c);
+        it.plane = 0;
+        it.q_row0 = s0;
+        it.q_len = s1 - s0;
+        int64_t k0 = 0, k1 = S;
+        if (trim(s0, s1, k0, k1, causal, window)) it.kv[it.n_kv++] = Range{k0, k1 - k0};
+        plan.items.push_back(it);
+        s0 = s1;
+      }
+      plan.n_launches = static_cast<int>(sizes.size());
+      plan.n_planes = 1;
+      plan.direct = true;
+      return SLOPE_OK;
+    }
     int64_t s0 = 0;
     for (size_t c = 0; c < sizes.size(); ++c) {
       const int64_t s1 = s0 + sizes[c];
@@ -298,12 +345,13 @@ slope_status build_base_plan(int64_t S, int n_chunks, slope_layout layout, const
 // is split into u items, one per query-head group (the ranks of one Ulysses group after the
 // all-to-all), which write the same partial planes.
 slope_status build_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
-                        int64_t window, Plan& plan) {
+                        int64_t window, unsigned flags, Plan& plan) {
   const unsigned word = static_cast<unsigned>(layout);
   if (word >> 16) return SLOPE_ERR_LAYOUT;
   const slope_layout base = static_cast<slope_layout>(word & 0xffu);
   const int u = static_cast<int>((word >> 8) & 0xffu);
-  slope_status st = build_base_plan(S, n_chunks, base, chunk_sizes, causal, window, plan);
+  slope_status st =
+      build_base_plan(S, n_chunks, base, chunk_sizes, causal, window, (flags & SLOPE_CP_FUSED) != 0, plan);
   if (st != SLOPE_OK || u <= 1) return st;
   if (base == SLOPE_LAYOUT_ULYSSES || u > kMaxRanks) {
     plan = Plan();
@@ -416,13 +464,21 @@ WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t dv, int n_planes
   return w;
 }
 
+// Known flags, alone or together where they mean something: bf16 partials exist only without
+// SLOPE_CP_FUSED, which keeps no partials.
+bool flags_valid(unsigned flags) {
+  const unsigned known = SLOPE_CP_BF16_PARTIALS | SLOPE_CP_FUSED;
+  if (flags & ~known) return false;
+  return (flags & known) != known;
+}
+
 // Every argument check of cp_prefill_impl, with no side effect; fills `plan`.
 slope_status cp_prefill_check(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int n_chunks,
                               slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
                               unsigned flags, const slope_tensor* out, const slope_tensor* lse,
                               const void* workspace, size_t workspace_bytes, Plan& plan) {
   slope_status st;
-  if (flags & ~static_cast<unsigned>(SLOPE_CP_BF16_PARTIALS)) return SLOPE_ERR_UNSUPPORTED;
+  if (!flags_valid(flags)) return SLOPE_ERR_UNSUPPORTED;
   if ((st = check_qkv(q)) != SLOPE_OK || (st = check_qkv(k)) != SLOPE_OK || (st = check_qkv(v)) != SLOPE_OK)
     return st;
   const int64_t S = q->shape[0], Hq = q->shape[1], dqk = q->shape[2];
@@ -434,7 +490,7 @@ slope_status cp_prefill_check(const slope_tensor* q, const slope_tensor* k, cons
   if ((st = check_out(out, S, Hq, dv, true)) != SLOPE_OK) return st;
   if (lse != nullptr && (st = check_lse(lse, Hq, S)) != SLOPE_OK) return st;
   if (S == 0) return SLOPE_ERR_SHAPE;
-  if ((st = build_plan(S, n_chunks, layout, chunk_sizes, causal, window, plan)) != SLOPE_OK) return st;
+  if ((st = build_plan(S, n_chunks, layout, chunk_sizes, causal, window, flags, plan)) != SLOPE_OK) return st;
   if (plan.n_planes > kMaxMerge) return SLOPE_ERR_UNSUPPORTED;
   if (Hkv % plan.n_head_groups != 0) return SLOPE_ERR_LAYOUT;  // whole KV heads per Ulysses rank
   if (plan.direct) {
@@ -713,7 +769,8 @@ slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, co
   if (Hq % Hkv != 0) return SLOPE_ERR_SHAPE;
   if (!attn_partial_supported(static_cast<int>(dqk), static_cast<int>(dv))) return SLOPE_ERR_UNSUPPORTED;
   if (window < 0 || window > kMaxSeq) return SLOPE_ERR_SHAPE;
-  if (std::llabs(q_off) > kMaxSeq || std::llabs(kv_off) > kMaxSeq) return SLOPE_ERR_SHAPE;
+  // every query and key position within [-2^28, 2^28]
+  if (q_off < -kMaxPos || q_off + Sq > kMaxPos || kv_off < -kMaxPos || kv_off + Skv > kMaxPos) return SLOPE_ERR_SHAPE;
   if ((st = check_out(out, Sq, Hq, dv, true)) != SLOPE_OK) return st;
   // bf16 rows are written 16 bytes at a time
   if (out->dtype == SLOPE_BF16 && (out->stride[0] % 8 || out->stride[1] % 8 || !aligned(out->data, 16)))
@@ -778,7 +835,7 @@ slope_status slope_lse_merge(const slope_tensor* outs, const slope_tensor* lses,
   if (n < 1 || n > kMaxMerge) return SLOPE_ERR_SHAPE;
   if (out->ndim != 3) return SLOPE_ERR_SHAPE;
   const int64_t S = out->shape[0], H = out->shape[1], dv = out->shape[2];
-  if (dv != 64 && dv != 128) return SLOPE_ERR_UNSUPPORTED;
+  if (!merge_dv_supported(dv)) return SLOPE_ERR_UNSUPPORTED;
   if (S < 0 || S > kMaxSeq || H <= 0 || H > 65535) return SLOPE_ERR_SHAPE;
   slope_status st;
   if ((st = check_out(out, S, H, dv, true)) != SLOPE_OK) return st;
@@ -814,10 +871,10 @@ slope_status slope_lse_merge(const slope_tensor* outs, const slope_tensor* lses,
 
 size_t slope_cp_prefill_workspace_size_ex(int64_t S, int64_t Hq, int64_t dv, int n_chunks, slope_layout layout,
                                           const int64_t* chunk_sizes, unsigned flags) {
-  if (S <= 0 || S > kMaxSeq || Hq <= 0 || (dv != 64 && dv != 128)) return 0;
-  if (flags & ~static_cast<unsigned>(SLOPE_CP_BF16_PARTIALS)) return 0;
+  if (S <= 0 || S > kMaxSeq || Hq <= 0 || !merge_dv_supported(dv)) return 0;
+  if (!flags_valid(flags)) return 0;
   Plan plan;
-  if (build_plan(S, n_chunks, layout, chunk_sizes, 1, 0, plan) != SLOPE_OK) return 0;
+  if (build_plan(S, n_chunks, layout, chunk_sizes, 1, 0, flags, plan) != SLOPE_OK) return 0;
   return workspace_layout(S, Hq, dv, plan.n_planes, flags, plan.direct).total;
 }
 
@@ -875,7 +932,7 @@ slope_status slope_cp_prefill_timed(const slope_tensor* q, const slope_tensor* k
   // count launches first so that a short event array is an argument error, not a partial run
   if (q != nullptr && q->ndim == 3) {
     Plan plan;
-    if (build_plan(q->shape[0], n_chunks, layout, chunk_sizes, causal, window, plan) == SLOPE_OK) {
+    if (build_plan(q->shape[0], n_chunks, layout, chunk_sizes, causal, window, 0u, plan) == SLOPE_OK) {
       int needed = 1;
       size_t i = 0;
       for (int l = 0; l < plan.n_launches; ++l) {
@@ -954,11 +1011,12 @@ slope_status slope_cp_prefill_host(const slope_tensor* q_host, const slope_tenso
   return SLOPE_OK;
 }
 
-int64_t slope_cp_prefill_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
-                              int64_t window, slope_plan_item* items, int64_t capacity, int32_t* n_launches,
-                              int32_t* n_planes) {
+int64_t slope_cp_prefill_plan_ex(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes,
+                                 int causal, int64_t window, unsigned flags, slope_plan_item* items, int64_t capacity,
+                                 int32_t* n_launches, int32_t* n_planes) {
+  if (!flags_valid(flags)) return SLOPE_ERR_UNSUPPORTED;
   Plan plan;
-  slope_status st = build_plan(S, n_chunks, layout, chunk_sizes, causal, window, plan);
+  slope_status st = build_plan(S, n_chunks, layout, chunk_sizes, causal, window, flags, plan);
   if (st != SLOPE_OK) return st;
   if (capacity > 0 && items == nullptr) return SLOPE_ERR_NULL;
   for (int64_t i = 0; i < static_cast<int64_t>(plan.items.size()) && i < capacity; ++i) {
@@ -980,6 +1038,13 @@ int64_t slope_cp_prefill_plan(int64_t S, int n_chunks, slope_layout layout, cons
   if (n_launches != nullptr) *n_launches = plan.n_launches;
   if (n_planes != nullptr) *n_planes = plan.n_planes;
   return static_cast<int64_t>(plan.items.size());
+}
+
+int64_t slope_cp_prefill_plan(int64_t S, int n_chunks, slope_layout layout, const int64_t* chunk_sizes, int causal,
+                              int64_t window, slope_plan_item* items, int64_t capacity, int32_t* n_launches,
+                              int32_t* n_planes) {
+  return slope_cp_prefill_plan_ex(S, n_chunks, layout, chunk_sizes, causal, window, 0u, items, capacity, n_launches,
+                                  n_planes);
 }
 
 slope_status slope_device_status(void* stream, int* site) {

@@ -74,7 +74,8 @@ struct K1Cfg {
   static constexpr int kKTileBytes = kQChunks * kChunkBytes;
   static constexpr int kVTileBytes = kVChunks * kChunkBytes;
   static constexpr int kSlotBytes = kKTileBytes > kVTileBytes ? kKTileBytes : kVTileBytes;
-  static constexpr int kSlots = DQK == 64 ? 8 : (DQK == 128 ? 4 : 2);
+  // 128 KB of K/V slots: 8 of 16 KB at d = 64, 4 of 32 KB with a 128-column K or V tile, 2 of 48 KB at 192
+  static constexpr int kSlots = 131072 / kSlotBytes;
   static constexpr int kNumBars = 1 + 2 * kSlots + 6 * kQTiles + 1 + 4 * kQTiles;
   // epilogue staging: 32-row x 32-column fp32 boxes (4 KB each, 128-byte swizzle), two per
   // softmax warp where shared memory allows (the second box is written while the first
@@ -932,16 +933,20 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 
 }  // namespace
 
+// (dqk, dv) in {64, 128, 192} x {64, 128}.  dv = 192 is not built: the two Q tiles' O
+// accumulators (2 x 192 TMEM columns) and their S tiles (2 x 128) would need 640 of the 512
+// columns of an SM's tensor memory.
 bool attn_partial_supported(int dqk, int dv) {
-  return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 64) || (dqk == 128 && dv == 128) ||
-         (dqk == 192 && dv == 128);
+  return (dqk == 64 || dqk == 128 || dqk == 192) && (dv == 64 || dv == 128);
 }
 
 cudaError_t launch_attn_partial(int dqk, int dv, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& to, const AttnParams& p, cudaStream_t stream) {
   if (dqk == 64 && dv == 64) return launch_impl<64, 64>(tq, tk, tv, to, p, stream);
+  if (dqk == 64 && dv == 128) return launch_impl<64, 128>(tq, tk, tv, to, p, stream);
   if (dqk == 128 && dv == 64) return launch_impl<128, 64>(tq, tk, tv, to, p, stream);
   if (dqk == 128 && dv == 128) return launch_impl<128, 128>(tq, tk, tv, to, p, stream);
+  if (dqk == 192 && dv == 64) return launch_impl<192, 64>(tq, tk, tv, to, p, stream);
   if (dqk == 192 && dv == 128) return launch_impl<192, 128>(tq, tk, tv, to, p, stream);
   return cudaErrorInvalidValue;
 }

@@ -96,6 +96,8 @@ cudaError_t launch_attn_partial(int dqk, int dv, const CUtensorMap& tq, const CU
                                 cudaStream_t stream);
 bool attn_partial_supported(int dqk, int dv);
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);
+// Head sizes the merge kernel is built for (64, 128 and 192).
+inline bool merge_dv_supported(long long dv) { return dv == 64 || dv == 128 || dv == 192; }
 cudaError_t launch_timeout_selftest(uint64_t limit_ns, int* status, cudaStream_t stream);
 int* device_status_ptr();  // per current device; nullptr on failure
 

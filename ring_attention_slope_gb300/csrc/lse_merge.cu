@@ -151,6 +151,7 @@ cudaError_t launch_impl(const MergeParams& p, cudaStream_t stream) {
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
   if (p.dv == 64) return p.out_bf16 ? launch_impl<64, true>(p, stream) : launch_impl<64, false>(p, stream);
   if (p.dv == 128) return p.out_bf16 ? launch_impl<128, true>(p, stream) : launch_impl<128, false>(p, stream);
+  if (p.dv == 192) return p.out_bf16 ? launch_impl<192, true>(p, stream) : launch_impl<192, false>(p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_symbols()
-    assert len(names) == 15, names
+    assert len(names) == 16, names
     for n in names:
         assert hasattr(lib, n), f"{n} declared in slope.h but not exported"
     assert sorted(names) == sorted(slope.EXPORTED)
@@ -135,7 +135,8 @@ def test_cp_prefill_ex_flags(lib):
         return lib.slope_cp_prefill_ex(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), n, 1, None, 1, 0, 0.0,
                                        flags, ctypes.byref(out), ctypes.byref(lse), 0x20000, ws_bytes, None)
 
-    assert call(2) == E_UNSUP
+    assert call(3) == E_UNSUP      # bf16 partials with the fused form, which keeps no partials
+    assert call(4) == E_UNSUP
     assert call(1 << 31) == E_UNSUP
     assert call(1, n=5) == E_LAYOUT
     lay = ctypes.c_int(1)
@@ -148,6 +149,33 @@ def test_cp_prefill_ex_flags(lib):
     assert w0 == 4 * S * Hq * d * 4 + lse_bytes and w1 == 4 * S * Hq * d * 2 + lse_bytes
     assert call(1, ws_bytes=w1 - 1) == E_WS
     assert call(0, ws_bytes=w1) == E_WS  # fp32 partials need the larger workspace
+    # the fused form keeps no partials: an lse plane only (used when lse is NULL)
+    w2 = lib.slope_cp_prefill_workspace_size_ex(S, Hq, d, 4, lay, None, 2)
+    assert w2 == S * Hq * 4
+    assert lib.slope_cp_prefill_workspace_size_ex(S, Hq, d, 4, lay, None, 3) == 0
+    assert call(2, ws_bytes=w2 - 1) == E_WS
+    assert call(2, n=5) == E_LAYOUT
+
+
+def test_attn_partial_position_bound(lib):
+    """Every query and key position lies in [-2^28, 2^28]; beyond it the call is refused before any launch
+    (the kernel takes position differences, less the window, in 32-bit integers)."""
+    Sq, Skv, Hq, Hkv, d = 300, 200, 8, 2, 64
+    q, k, v = _t([Sq, Hq, d]), _t([Skv, Hkv, d]), _t([Skv, Hkv, d])
+    out, lse = _t([Sq, Hq, d], dtype=1), _t([Hq, Sq], dtype=1)
+
+    def call(q_off, kv_off, window=0):
+        return lib.slope_attn_partial(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), q_off, kv_off, 1, window,
+                                      0.0, ctypes.byref(out), ctypes.byref(lse), None)
+
+    M = 1 << 28
+    assert call(1 << 30, -(1 << 30)) == E_SHAPE          # the differences would pass 2^31
+    assert call(M - Sq + 1, 0) == E_SHAPE                 # last query position 2^28 + 1 - 1 = 2^28 ... + 1
+    assert call(-M - 1, 0) == E_SHAPE
+    assert call(0, M - Skv + 1) == E_SHAPE
+    assert call(0, -M - 1) == E_SHAPE
+    assert call(0, 0, window=(1 << 30) + 1) == E_SHAPE
+    assert call(-(1 << 62), 0) == E_SHAPE
 
 
 def test_empty_inputs_are_no_ops(lib):

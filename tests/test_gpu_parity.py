@@ -96,6 +96,10 @@ PARTIAL_CASES = [
     (270, 513, 3, 3, 192, 128, 243, 0, True, 0),
     (1, 1, 1, 1, 64, 64, 0, 0, True, 0),
     (129, 1, 2, 1, 64, 64, 5, 4, True, 0),
+    (300, 410, 4, 2, 64, 128, 110, 0, True, 0),       # dqk 64, dv 128 (P over S, turns)
+    (384, 384, 2, 2, 64, 128, 0, 0, True, 77),
+    (270, 513, 3, 3, 192, 64, 243, 0, True, 0),       # dqk 192, dv 64 (separate P)
+    (333, 333, 4, 4, 192, 64, 0, 0, False, 0),
 ]
 
 
@@ -112,7 +116,7 @@ def test_attn_partial_matches_oracle(case):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("d,dv", [(64, 64), (128, 64), (128, 128), (192, 128)])
+@pytest.mark.parametrize("d,dv", [(64, 64), (64, 128), (128, 64), (128, 128), (192, 64), (192, 128)])
 def test_attn_partial_score_jumps_inside_a_key_tile(causal, d, dv):
     """Keys whose scores jump by tens of log2 units inside one 128-key tile and again in
     later tiles: the running max moves many times and the row sum and O are rescaled
@@ -145,6 +149,24 @@ def test_attn_partial_no_keys_and_future_keys():
     assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
 
 
+@pytest.mark.parametrize("q_off,kv_off,causal,window", [
+    (2**28 - 300, 2**28 - 300 - 250, True, 0),       # the last positions allowed
+    (-2**28 + 250, -2**28, True, 100),               # the first positions allowed
+    (2**28 - 300, -2**28, False, 0),                 # query - key position differences near 2^29
+    (-2**28, 2**28 - 250, False, 2**30),             # keys all "after" the queries, the largest window
+    (2**28 - 300, 2**28 - 450, True, 2**30),
+])
+def test_attn_partial_extreme_positions(q_off, kv_off, causal, window):
+    """Positions at the ends of the accepted range [-2^28, 2^28]: the kernel's 32-bit position differences
+    (less the window) do not overflow, and the masks match the oracle's 64-bit ones."""
+    q, k, v = qkv(300, 4, 2, 64, 64, seed=q_off % 9973, Skv=250)
+    out, lse = slope.attn_partial(q, k, v, q_off=q_off, kv_off=kv_off, causal=causal, window=window)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), q_pos0=q_off, kv_pos0=kv_off, causal=causal, window=window)
+    compare(out.cpu(), lse.cpu(), ro, rl, f"positions {q_off} {kv_off}")
+    assert slope.device_status() == (0, 0)
+
+
 def test_attn_partial_window1_is_exact_identity():
     q, k, v = qkv(300, 2, 1, 64, 64, seed=6)
     out, lse = slope.attn_partial(q, k, v, causal=True, window=1)
@@ -173,7 +195,7 @@ def test_attn_partial_strided_views():
 
 # ---------------------------------------------------------------- merge
 
-@pytest.mark.parametrize("dv", [64, 128])
+@pytest.mark.parametrize("dv", [64, 128, 192])
 @pytest.mark.parametrize("n", [1, 2, 5, 16, 32])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_lse_merge_matches_oracle(dv, n, out_dtype):
@@ -264,11 +286,12 @@ def test_cp_prefill_mla_shape_small():
 
 # ---------------------------------------------------------------- full-size workloads, sampled rows/heads
 
-def check_full_workload(w, window, rows_random=4096, bf16_partials=False):
+def check_full_workload(w, window, rows_random=4096, bf16_partials=False, fused=False, sizes=None):
     q, k, v = wl.workload_qkv(w, device="cuda")
-    sizes = wl.chunk_sizes(w)
-    n = wl.n_chunks(w)
-    out, lse = slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window, bf16_partials=bf16_partials)
+    sizes = wl.chunk_sizes(w) if sizes is None else sizes
+    n = len(sizes) if sizes is not None else wl.n_chunks(w)
+    out, lse = slope.cp_prefill(q, k, v, n, w.layout, chunk_sizes=sizes, window=window, bf16_partials=bf16_partials,
+                                fused=fused)
     torch.cuda.synchronize()
     assert slope.device_status() == (0, 0)
     rows = wl.sample_rows(w, n_random=rows_random)
@@ -277,7 +300,7 @@ def check_full_workload(w, window, rows_random=4096, bf16_partials=False):
     ro, rl = oracle.attention(qc, kc, vc, causal=True, window=window, rows=rows, heads=heads)
     og = out[torch.from_numpy(rows).cuda()][:, heads].float().cpu()
     lg = lse[heads][:, torch.from_numpy(rows).cuda()].cpu()
-    compare(og, lg, ro, rl, f"{w.name} W={window} bf16_partials={bf16_partials}")
+    compare(og, lg, ro, rl, f"{w.name} W={window} bf16_partials={bf16_partials} fused={fused}")
     # properties at every row: finite outputs, lse >= the log of... finite and bounded
     assert torch.isfinite(out.float()).all()
     assert torch.isfinite(lse).all()
@@ -562,3 +585,58 @@ def test_cp_prefill_ulysses_ring_equals_the_ring(layout, n, u, window, sizes, di
     assert torch.equal(o, bo) and torch.equal(l, bl)
     ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, window=window)
     compare(o.cpu(), l.cpu(), ro, rl, f"ulysses x ring {layout} n={n} u={u} W={window}")
+
+
+# ---------------------------------------------------------------- fused layouts (slope_cp_prefill_ex, SLOPE_CP_FUSED)
+
+@pytest.mark.parametrize("layout,n,u,window,sizes,dims", [
+    ("zigzag", 4, 1, 0, None, (8, 4, 64, 64)), ("zigzag", 8, 1, 100, None, (8, 4, 64, 64)),
+    ("contiguous", 4, 1, 0, None, (8, 4, 64, 64)), ("zigzag", 2, 2, 0, None, (8, 4, 128, 128)),
+    ("chunked", 3, 1, 0, [700, 1, 1347], (8, 4, 64, 64)), ("chunked", 2, 1, 300, [1000, 1048], (4, 4, 192, 128)),
+    ("chunked", 4, 2, 0, [300, 700, 548, 500], (4, 2, 64, 128)), ("zigzag", 16, 1, 0, None, (4, 1, 192, 64))])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_cp_prefill_fused_matches_oracle(layout, n, u, window, sizes, dims, out_dtype):
+    """SLOPE_CP_FUSED: each rank's (or chunk's) query rows over all their visible keys in one item, written
+    directly.  It matches the oracle and the partials-and-merge result; without a window every item's key
+    range starts at key 0, like the single launch over the whole sequence, and the result is bit-identical
+    to that launch."""
+    S = 2048
+    Hq, Hkv, dqk, dv = dims
+    q, k, v = qkv(S, Hq, Hkv, dqk, dv, seed=131 + n + dqk + u, scale_v=0.7)
+    lay = slope.layout_code(layout, u)
+    o, l = slope.cp_prefill(q, k, v, n, lay, chunk_sizes=sizes, window=window, out_dtype=out_dtype, fused=True)
+    mo, ml = slope.cp_prefill(q, k, v, n, lay, chunk_sizes=sizes, window=window, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert slope.device_status() == (0, 0)
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, window=window)
+    compare(o.float().cpu(), l.cpu(), ro, rl, f"fused {layout} n={n} u={u} W={window} {out_dtype}")
+    compare(o.float().cpu(), l.cpu(), mo.float().cpu().double().numpy(), ml.cpu().double().numpy(),
+            f"fused vs partials+merge {layout} n={n}")
+    if window == 0:
+        fo = torch.empty_like(o)
+        fl = torch.empty_like(l)
+        slope.attn_partial(q, k, v, causal=True, out=fo, lse=fl)
+        torch.cuda.synchronize()
+        assert torch.equal(o, fo) and torch.equal(l, fl)
+
+
+def test_cp_prefill_fused_without_lse_uses_the_workspace_plane():
+    S, Hq, Hkv, d, n = 1024, 4, 2, 64, 4
+    q, k, v = qkv(S, Hq, Hkv, d, d, seed=141)
+    nbytes = slope.cp_prefill_workspace_size(S, Hq, d, n, "zigzag", fused=True)
+    assert nbytes == S * Hq * 4
+    ws = torch.empty((nbytes,), dtype=torch.uint8, device="cuda")
+    o, l = slope.cp_prefill(q, k, v, n, "zigzag", workspace=ws, want_lse=False, fused=True)
+    torch.cuda.synchronize()
+    assert l is None
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True)
+    lse_ws = ws.view(torch.float32).view(S, Hq).T.cpu()
+    compare(o.float().cpu(), lse_ws, ro, rl, "fused, lse in the workspace")
+
+
+def test_full_causal_gqa_s32k_zigzag8_fused():
+    check_full_workload(wl.WORKLOADS[1], 0, rows_random=2048, fused=True)
+
+
+def test_full_chunked_prefill_s64k_fused():
+    check_full_workload(wl.WORKLOADS[2], 0, rows_random=2048, fused=True)

@@ -174,3 +174,50 @@ def test_ulysses_ring_plan_errors():
         slope.cp_prefill_plan(256, 4, slope.layout_code("zigzag", 33))   # more than 32 groups
     with pytest.raises(slope.SlopeError):
         slope.cp_prefill_plan(256, 4, 1 | (1 << 16))                      # bits above the degree
+
+
+@pytest.mark.parametrize("layout,N,sizes", [("zigzag", 1, None), ("zigzag", 4, None), ("zigzag", 16, None),
+                                            ("contiguous", 3, None), ("contiguous", 8, None),
+                                            ("chunked", 3, [100, 250, 170]), ("chunked", 5, None)])
+@pytest.mark.parametrize("window", [0, 1, 37, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_fused_plan_covers_each_visible_pair_once(layout, N, sizes, window, causal):
+    """SLOPE_CP_FUSED: one item per query sub-chunk (ring) or chunk, each over one key range, writing the
+    final output directly (one plane); together they cover every visible pair exactly once, and every
+    query row belongs to exactly one item."""
+    S = 520 if layout == "chunked" else (2 * N if layout == "zigzag" else N) * 24
+    items, n_launches, n_planes = slope.cp_prefill_plan(S, N, layout, chunk_sizes=sizes, causal=causal,
+                                                        window=window, fused=True)
+    assert n_planes == 1 and n_launches == N
+    assert all(it["plane"] == 0 and len(it["kv"]) <= 1 for it in items)
+    cnt, vis = coverage(items, S, window, causal)
+    assert np.array_equal(cnt, vis.astype(np.int32)), "some visible pair missing or counted twice"
+    rows = np.zeros(S, dtype=np.int32)
+    for it in items:
+        rows[it["q_row0"]:it["q_row0"] + it["q_len"]] += 1
+    assert np.all(rows == 1)
+    # each item's range is exactly the union of the keys its rows see (nothing wider)
+    for it in items:
+        q0, q1 = it["q_row0"], it["q_row0"] + it["q_len"]
+        seen = np.flatnonzero(vis[q0:q1].any(axis=0))
+        if it["kv"]:
+            (k0, kl), = it["kv"]
+            assert k0 == seen[0] and k0 + kl == seen[-1] + 1
+        else:
+            assert seen.size == 0
+    # the ring's items per rank: zigzag r owns sub-chunks r and 2N-1-r
+    if layout == "zigzag":
+        sub = S // (2 * N)
+        for r in range(N):
+            mine = sorted(it["q_row0"] // sub for it in items if it["launch"] == r)
+            assert mine == sorted({r, 2 * N - 1 - r})
+
+
+def test_plan_ex_flags():
+    """plan_ex with flags 0 is the plain plan; conflicting or unknown flags are refused."""
+    lib = slope.load()
+    assert lib.slope_cp_prefill_plan_ex(1024, 4, 1, None, 1, 0, 3, None, 0, None, None) == -8
+    assert lib.slope_cp_prefill_plan_ex(1024, 4, 1, None, 1, 0, 8, None, 0, None, None) == -8
+    a, la, pa = slope.cp_prefill_plan(1024, 4, "zigzag", window=64)
+    b = lib.slope_cp_prefill_plan(1024, 4, 1, None, 1, 64, None, 0, None, None)
+    assert len(a) == b and la == 4 and pa == 4
