@@ -484,6 +484,8 @@ def run_extra(ctx, w, window, args):
     if not args.no_variants:
         rec["fused_layout"] = run_fused_layout(slope, torch, w, n, sizes, window, q, k, v, out, lse, ctx.stream, sub,
                                                ctx.barrier, ctx.dist)
+    if w.layout == "chunked" and not args.no_variants:
+        rec["dck"] = run_dck(slope, torch, w, window, q, k, v, out, lse, ctx.stream, sub, ctx.barrier, ctx.dist)
     if not args.no_e2e and w.dqk != w.dv:
         rec["e2e"] = run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, ctx.stream,
                              argparse.Namespace(**{**vars(args), "steps": max(steps, 10)}), ctx.barrier, ctx.dist)
@@ -529,17 +531,10 @@ def merge_bytes_per_launch(slope, w, n, sizes, window):
     return float(w.Hq * (reads + w.S * (w.dv * 2 + 4)))
 
 
-def k1_bytes_per_launch(slope, w, n, sizes, window):
-    """Algorithmic DRAM bytes of an average attention launch of one step, from the plan.
-
-    Plan launches (ring steps, chunks) are grouped into kernel launches by the library's rule:
-    consecutive steps share a launch while their live items fit in 32 (a plane none of whose
-    items sees a key is dropped).  Per kernel launch: each distinct Q row that sees a key and
-    each distinct K/V row is read once, and every item writes its fp32 partial out + lse for
-    rows that see a key, or its lse alone for rows that see none.
-    Returns (bytes per launch, launches per step).
-    """
-    items, n_launch, _ = slope.cp_prefill_plan(w.S, n, w.layout, chunk_sizes=sizes, causal=True, window=window)
+def launch_groups(items, n_launch):
+    """Plan launches (ring steps, chunks, ranks) grouped into kernel launches by the library's rule:
+    consecutive ones share a launch while their items fit in 32; a partial plane none of whose items sees
+    a key is dropped (plane 0 is always kept)."""
     live_planes = {0} | {it["plane"] for it in items if it["kv"]}
     by_launch = {}
     for it in items:
@@ -554,6 +549,21 @@ def k1_bytes_per_launch(slope, w, n, sizes, window):
         cur = cur + step
     if cur:
         groups.append(cur)
+    return groups
+
+
+def k1_bytes_per_launch(slope, w, n, sizes, window):
+    """Algorithmic DRAM bytes of an average attention launch of one step, from the plan.
+
+    Plan launches (ring steps, chunks) are grouped into kernel launches by the library's rule:
+    consecutive steps share a launch while their live items fit in 32 (a plane none of whose
+    items sees a key is dropped).  Per kernel launch: each distinct Q row that sees a key and
+    each distinct K/V row is read once, and every item writes its fp32 partial out + lse for
+    rows that see a key, or its lse alone for rows that see none.
+    Returns (bytes per launch, launches per step).
+    """
+    items, n_launch, _ = slope.cp_prefill_plan(w.S, n, w.layout, chunk_sizes=sizes, causal=True, window=window)
+    groups = launch_groups(items, n_launch)
     total = 0.0
     for g in groups:
         qrows = np.zeros(w.S, dtype=bool)
@@ -610,10 +620,33 @@ def run_fused_layout(slope, torch, w, n, sizes, window, q, k, v, out, lse, strea
                          fused=True)
 
     ms, world = time_variant(torch, step, stream, args, barrier, dist)
-    _, n_launch, _ = slope.cp_prefill_plan(w.S, n, w.layout, chunk_sizes=sizes, window=window, fused=True)
+    items, n_launch, _ = slope.cp_prefill_plan(w.S, n, w.layout, chunk_sizes=sizes, window=window, fused=True)
     return {"value": job_tflops(workload_flops(w, window), args.steps, world, ms), "unit": UNIT,
             "ms_per_step": ms / args.steps, "api": "slope_cp_prefill_ex(SLOPE_CP_FUSED)",
-            "gpu_launches_per_step": n_launch}
+            "gpu_launches_per_step": len(launch_groups(items, n_launch))}
+
+
+def run_dck(slope, torch, w, window, q, k, v, out, lse, stream, args, barrier, dist):
+    """The chunked workload with dynamic chunk sizes (slope_dck_chunk_sizes: initial 12288, smoothing 0.65),
+    as partials + merge and in the fused form."""
+    sizes = slope.dck_chunk_sizes(w.S, 12288, 0.65)
+    n = len(sizes)
+    res = {"chunks": n, "first": sizes[0], "last_full": sizes[-2] if n > 1 else sizes[0],
+           "api": "slope_dck_chunk_sizes(S, 12288, 0.65) -> slope_cp_prefill(SLOPE_LAYOUT_CHUNKED)"}
+    ws = torch.empty((slope.cp_prefill_workspace_size(w.S, w.Hq, w.dv, n, "chunked", sizes),), dtype=torch.uint8,
+                     device="cuda")
+
+    def step():
+        slope.cp_prefill(q, k, v, n, "chunked", chunk_sizes=sizes, window=window, out=out, lse=lse, workspace=ws)
+
+    ms, world = time_variant(torch, step, stream, args, barrier, dist)
+    res["value"] = job_tflops(workload_flops(w, window), args.steps, world, ms)
+    res["unit"] = UNIT
+    res["ms_per_step"] = ms / args.steps
+    del ws
+    res["fused_layout"] = run_fused_layout(slope, torch, w, n, sizes, window, q, k, v, out, lse, stream, args,
+                                           barrier, dist)
+    return res
 
 
 def time_variant(torch, step, stream, args, barrier, dist):
@@ -696,20 +729,52 @@ def run_e2e(slope, torch, w, n, sizes, window, q, k, v, ws, stream, args, barrie
         step(i)
     torch.cuda.synchronize()
     barrier()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.15)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(s_in)
     for i in range(args.steps):
         step(i)
     b.record(s_out)
     torch.cuda.synchronize()
+    clocks = sampler.stop()
     ms = max_over_ranks(a.elapsed_time(b), dist, "cuda")
     world = dist.get_world_size() if dist is not None else 1
     val = job_tflops(workload_flops(w, window), args.steps, world, ms)
     h2d = int(hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2)
     d2h = int(sets[0]["hout"].numel() * 2 + sets[0]["hlse"].numel() * 4)
+
+    # the copies alone, on the same buffers and streams: with the copies overlapped, a step takes about
+    # the longest of the input copies, the compute and the output copies
+    def copy_ms(fn, st, reps=3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            fn()
+        e1.record(st)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    b0 = sets[0]
+
+    def h2d_copy():
+        with torch.cuda.stream(s_in):
+            b0["q"].copy_(hq, non_blocking=True)
+            b0["k"].copy_(hk, non_blocking=True)
+            b0["v"].copy_(hv, non_blocking=True)
+
+    def d2h_copy():
+        with torch.cuda.stream(s_out):
+            b0["hout"].copy_(b0["out"], non_blocking=True)
+            b0["hlse"].copy_(b0["lse"], non_blocking=True)
+
+    h2d_ms, d2h_ms = copy_ms(h2d_copy, s_in), copy_ms(d2h_copy, s_out)
     return {"value": val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": ms / args.steps, "api": "slope_cp_prefill_host",
-            "overlap": "2 device-buffer sets; input copies, compute and output copies on 3 streams"}
+            "overlap": "2 device-buffer sets; input copies, compute and output copies on 3 streams",
+            "h2d_alone_ms": h2d_ms, "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9,
+            "d2h_alone_ms": d2h_ms, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9, "clocks": clocks}
 
 
 def main():

@@ -383,6 +383,33 @@ SLOPE_API int64_t slope_cp_prefill_plan_ex(int64_t S, int n_chunks, slope_layout
                                            int64_t capacity, int32_t* n_launches, int32_t* n_planes);
 
 /*
+ * Dynamic chunk sizing for SLOPE_LAYOUT_CHUNKED (host only, no GPU needed).
+ *
+ * The SGLang pipeline-parallelism article (TL;DR, caption of its throughput
+ * figure) runs chunked prefill with dynamic chunking from an initial chunk of
+ * 12288 tokens with a smoothing factor of 0.65, but stops before giving the
+ * algorithm.  This call implements one reading of those two numbers: later
+ * chunks shrink as the key prefix grows, towards the size whose attention cost
+ * (visible query-key pairs: row i sees i + 1 keys, or min(i + 1, window))
+ * equals the first chunk's, smoothed exponentially with factor sigma:
+ *   n_0 = min(initial, S);
+ *   n_c = round(sigma * n*(s_c) + (1 - sigma) * n_{c-1}), then rounded down to
+ *         a multiple of align (at least align), the last chunk clipped to S,
+ * where s_c is the chunk's first token and n*(s) the largest n >= 1 with
+ * cost(s, n) <= cost(0, n_0).  Sizes never grow; sigma = 0 gives fixed chunks
+ * of n_0, sigma = 1 chunks of equal cost.
+ *
+ *   S (1..2^30), initial >= 1, 0 <= sigma <= 1, window >= 0 (0 = none),
+ *   1 <= align <= initial: else SLOPE_ERR_SHAPE.  sizes: host array of
+ *   `capacity` entries (NULL when capacity is 0), filled with the first
+ *   min(count, capacity) sizes.
+ * Returns the number of chunks (their sizes sum to S), or a negative
+ * slope_status.  Pass the sizes to slope_cp_prefill as chunk_sizes.
+ */
+SLOPE_API int64_t slope_dck_chunk_sizes(int64_t S, int64_t initial, double sigma, int64_t window, int64_t align,
+                                        int64_t* sizes, int64_t capacity);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device: SLOPE_OK, or SLOPE_ERR_TIMEOUT if a bounded kernel wait ran
  * out since the last query (the kernel that saw it skipped its remaining work

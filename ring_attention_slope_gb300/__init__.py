@@ -24,7 +24,7 @@ from ._build import LIB_PATH
 __all__ = [
     "SlopeError", "load", "build", "attn_partial", "lse_merge", "cp_prefill", "cp_prefill_timed",
     "cp_prefill_workspace_size", "cp_prefill_plan", "device_status", "timeout_selftest", "LAYOUTS", "version",
-    "cp_prefill_static_scratch",
+    "cp_prefill_static_scratch", "dck_chunk_sizes",
 ]
 
 LAYOUTS = {"contiguous": 0, "zigzag": 1, "chunked": 2, "ulysses": 3}
@@ -57,7 +57,7 @@ EXPORTED = ["slope_attn_partial", "slope_lse_merge", "slope_cp_prefill", "slope_
             "slope_cp_prefill_timed", "slope_cp_prefill_plan", "slope_device_status",
             "slope_debug_timeout_selftest", "slope_status_string", "slope_version", "slope_last_error",
             "slope_cp_prefill_static_scratch", "slope_cp_prefill_host", "slope_cp_prefill_ex",
-            "slope_cp_prefill_workspace_size_ex", "slope_cp_prefill_plan_ex"]
+            "slope_cp_prefill_workspace_size_ex", "slope_cp_prefill_plan_ex", "slope_dck_chunk_sizes"]
 
 # flags of slope_cp_prefill_ex (include/slope.h)
 CP_BF16_PARTIALS = 1
@@ -98,6 +98,8 @@ def load():
     lib.slope_cp_prefill_plan_ex.argtypes = [i64, c_int, c_int, P(i64), c_int, i64, ctypes.c_uint, P(SlopePlanItem),
                                              i64, P(ctypes.c_int32), P(ctypes.c_int32)]
     lib.slope_cp_prefill_plan_ex.restype = i64
+    lib.slope_dck_chunk_sizes.argtypes = [i64, i64, ctypes.c_double, i64, i64, P(i64), i64]
+    lib.slope_dck_chunk_sizes.restype = i64
     lib.slope_device_status.argtypes = [vp, P(c_int)]
     lib.slope_device_status.restype = c_int
     lib.slope_debug_timeout_selftest.argtypes = [ctypes.c_uint64, vp]
@@ -403,6 +405,21 @@ def cp_prefill_plan(S, n_chunks, layout, *, chunk_sizes=None, causal=True, windo
                     "kv": [(it.kv_row0[r], it.kv_len[r]) for r in range(it.n_kv)],
                     "head_group": it.head_group, "n_head_groups": it.n_head_groups})
     return res, nl.value, npl.value
+
+
+def dck_chunk_sizes(S, initial=12288, sigma=0.65, *, window=0, align=1):
+    """Dynamic chunk sizes for the chunked layout (slope_dck_chunk_sizes): from an initial chunk, later
+    chunks move towards the size whose attention cost equals the first chunk's, smoothed with factor sigma.
+    Returns a list of ints summing to S."""
+    lib = load()
+    n = lib.slope_dck_chunk_sizes(int(S), int(initial), float(sigma), int(window), int(align), None, 0)
+    if n < 0:
+        raise SlopeError(int(n), "slope_dck_chunk_sizes")
+    arr = (ctypes.c_int64 * n)()
+    n2 = lib.slope_dck_chunk_sizes(int(S), int(initial), float(sigma), int(window), int(align),
+                                   ctypes.cast(arr, ctypes.POINTER(ctypes.c_int64)), n)
+    assert n2 == n
+    return [int(x) for x in arr]
 
 
 def device_status(stream=None):

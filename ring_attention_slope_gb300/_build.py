@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libslope.so")
 
-SOURCES = ["api.cu", "attn_partial.cu", "lse_merge.cu", "status.cu"]
+SOURCES = ["api.cu", "attn_partial.cu", "lse_merge.cu", "status.cu", "dck.cpp"]
 HEADERS = ["kernels.cuh", "sm103_ptx.cuh", "waits.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -23,16 +23,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t elect_one_lane() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "elect.sync _|p, 0xffffffff;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(pred));
-  return pred;
-}
-
 // ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -147,30 +137,10 @@ __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D(tmem) = A(smem) * B(smem) [+ D]
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D(tmem) = A(tmem) * B(smem) [+ D]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Same MMAs with the 64-bit descriptors given as (low, high) words, so that a
-// caller can keep the high word fixed and step the start address in the low word.
+// D(tmem) = A * B [+ D] on the tensor cores (kind::f16: bf16 operands, fp32 accumulator),
+// one instruction issued by one thread.  The 64-bit descriptors are given as (low, high)
+// words, so that a caller can keep the high word fixed and step the start address in the
+// low word.  mma_ss_lh: A and B in shared memory; mma_ts_lh: A in tensor memory.
 __device__ __forceinline__ void mma_ss_lh(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -250,18 +220,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -282,25 +240,16 @@ __device__ __forceinline__ void reg_fence(float& x) { asm volatile("" : "+f"(x))
 
 // ----------------------------------------------------------------- descriptors
 
-// Shared-memory matrix descriptor (tcgen05 form): start address, leading and
-// stride byte offsets (16-byte units), descriptor version 1 at bit 46, and the
-// swizzle mode in bits 61-63 (2 = 128-byte swizzle).  Tiles are 1024-byte
-// aligned so the base-offset field stays 0.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
-                                              uint32_t swizzle_mode) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(swizzle_mode & 7u) << 61;
-  return d;
-}
+// Shared-memory matrix descriptor (tcgen05 form), kept as two 32-bit words: the start
+// address (16-byte units, bits 0-13) and leading byte offset (16-byte units, bits 16-29)
+// in the low word; the stride byte offset (bits 32-45), descriptor version 1 (bit 46)
+// and the swizzle mode (bits 61-63, 2 = 128-byte swizzle) in the high word.  Tiles are
+// 1024-byte aligned so the base-offset field stays 0.
 constexpr uint32_t kSwizzle128B = 2;
 
-// Low / high 32-bit words of smem_desc(): the start address lives in bits 0-13 of
-// the low word, so adding (byte offset >> 4) to it steps through a tile as long as
-// the address stays below 256 KB (always true for shared memory).
+// Low / high words of the descriptor: the start address lives in bits 0-13 of the low
+// word, so adding (byte offset >> 4) to it steps through a tile as long as the address
+// stays below 256 KB (always true for shared memory).
 __device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
@@ -320,18 +269,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// ----------------------------------------------------------------- register budget
-
-// Warpgroup-wide register re-allocation (all 128 threads of the warpgroup execute it).
-template <uint32_t N>
-__device__ __forceinline__ void regs_increase() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void regs_decrease() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // ----------------------------------------------------------------- math
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -343,26 +280,6 @@ __device__ __forceinline__ float lg2_approx(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-// Packed fp32 pair arithmetic (one instruction for two lanes of data).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t d, ra, rb, rc;
-  asm("mov.b64 %0, {%1,%2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1,%2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1,%2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(ra), "l"(rb), "l"(rc));
-  float2 r;
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
-  return r;
-}
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-  uint64_t d, ra, rb;
-  asm("mov.b64 %0, {%1,%2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1,%2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(ra), "l"(rb));
-  float2 r;
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
-  return r;
 }
 // One pair of softmax elements: x = s * sl2 - m (packed FMA), p = 2^x (two MUFU ops),
 // acc += p (packed add, accumulator kept as a 64-bit register pair), and p packed to

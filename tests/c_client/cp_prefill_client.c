@@ -116,7 +116,21 @@ int main(void) {
     if (fabs(a - b) > worst) worst = fabs(a - b);
   }
   CHECK(worst <= 2e-2);
-  printf("ok %.3e %s\n", worst, slope_version());
+  /* the log-sum-exps of both calls: finite (every causal row sees itself) and within 1e-3 */
+  float* l1 = malloc((size_t)HQ * S * 4);
+  float* l2 = malloc((size_t)HQ * S * 4);
+  CHECK(l1 && l2);
+  CHECK(cudaMemcpy(l1, dl1, (size_t)HQ * S * 4, cudaMemcpyDeviceToHost) == cudaSuccess);
+  CHECK(cudaMemcpy(l2, dl2, (size_t)HQ * S * 4, cudaMemcpyDeviceToHost) == cudaSuccess);
+  double worst_lse = 0.0;
+  for (size_t i = 0; i < (size_t)HQ * S; ++i) {
+    CHECK(isfinite(l1[i]) && isfinite(l2[i]));
+    if (fabs((double)l1[i] - (double)l2[i]) > worst_lse) worst_lse = fabs((double)l1[i] - (double)l2[i]);
+  }
+  CHECK(worst_lse <= 1e-3);
+  free(l1);
+  free(l2);
+  printf("ok %.3e %.3e %s\n", worst, worst_lse, slope_version());
   cudaFree(dq);
   cudaFree(dk);
   cudaFree(dv);

@@ -295,6 +295,11 @@ def check_full_workload(w, window, rows_random=4096, bf16_partials=False, fused=
     torch.cuda.synchronize()
     assert slope.device_status() == (0, 0)
     rows = wl.sample_rows(w, n_random=rows_random)
+    if sizes is not None:  # the first and last rows of every chunk actually used
+        edges = np.cumsum([0] + list(sizes))
+        extra = [np.arange(a, min(b, a + 64)) for a, b in zip(edges[:-1], edges[1:])]
+        extra += [np.arange(max(a, b - 64), b) for a, b in zip(edges[:-1], edges[1:])]
+        rows = np.unique(np.concatenate([rows] + extra)).astype(np.int64)
     heads = wl.sample_heads(w)
     qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
     ro, rl = oracle.attention(qc, kc, vc, causal=True, window=window, rows=rows, heads=heads)
@@ -640,3 +645,25 @@ def test_full_causal_gqa_s32k_zigzag8_fused():
 
 def test_full_chunked_prefill_s64k_fused():
     check_full_workload(wl.WORKLOADS[2], 0, rows_random=2048, fused=True)
+
+
+# ---------------------------------------------------------------- dynamic chunk sizes (slope_dck_chunk_sizes)
+
+def test_full_chunked_prefill_s64k_dck():
+    """The 64K GQA workload chunked by the dynamic sizes (initial 12288, sigma 0.65): 27 chunks shrinking
+    from 12288 to about 1200 tokens, partials and merge, against the oracle on sampled rows."""
+    w = wl.WORKLOADS[2]
+    sizes = slope.dck_chunk_sizes(w.S, 12288, 0.65)
+    assert len(sizes) > 6 and sizes[0] == 12288
+    check_full_workload(w, 0, rows_random=2048, sizes=sizes)
+
+
+def test_full_mla_s64k_dck_fused():
+    """The MLA-shaped workload chunked by the dynamic sizes, in the fused form (one item per chunk)."""
+    w = wl.WORKLOADS[4]
+    check_full_workload(w, 0, rows_random=1024, sizes=slope.dck_chunk_sizes(w.S), fused=True)
+
+
+def test_full_mla_s64k_dck():
+    w = wl.WORKLOADS[4]
+    check_full_workload(w, 0, rows_random=1024, sizes=slope.dck_chunk_sizes(w.S))
