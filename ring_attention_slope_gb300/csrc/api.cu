@@ -381,9 +381,16 @@ double item_work(const PItem& it, int causal) {
   return w / it.n_hg;
 }
 
+// The attention kernel pairs two query heads of one KV group on the same 128 rows as the two
+// Q tiles of a work tile when a KV head serves an even number of query heads (both tiles then
+// take the same steps); otherwise its Q tiles are 256 consecutive rows of one head.
+bool pair_heads(int64_t Hq, int64_t Hkv) { return (Hq / Hkv) % 2 == 0; }
+
 // Packs items into launch parameter blocks (<= kMaxItems each), heaviest first.  Returns
 // false if a block has more work tiles than a launch indexes (2^31 - 1).
-bool pack_items(std::vector<PItem> items, int causal, int64_t Hq, std::vector<std::vector<WorkItem>>& out) {
+bool pack_items(std::vector<PItem> items, int causal, int64_t Hq, bool pair,
+                std::vector<std::vector<WorkItem>>& out) {
+  const int64_t rows_per_tile = pair ? kBlockM : kRowsPerCta;
   std::stable_sort(items.begin(), items.end(),
                    [&](const PItem& a, const PItem& b) { return item_work(a, causal) > item_work(b, causal); });
   out.clear();
@@ -400,11 +407,11 @@ bool pack_items(std::vector<PItem> items, int causal, int64_t Hq, std::vector<st
       w.n_kv = s.n_kv;
       for (int r = 0; r < s.n_kv; ++r) w.kv[r] = KvRange{static_cast<int32_t>(s.kv[r].row0),
                                                         static_cast<int32_t>(s.kv[r].len)};
-      w.n_blocks = static_cast<int32_t>((s.q_len + kRowsPerCta - 1) / kRowsPerCta);
+      w.n_blocks = static_cast<int32_t>((s.q_len + rows_per_tile - 1) / rows_per_tile);
       w.h_begin = static_cast<int32_t>(s.hg * (Hq / s.n_hg));
       w.h_count = static_cast<int32_t>(Hq / s.n_hg);
       w.tile_begin = static_cast<int32_t>(begin);
-      begin += static_cast<int64_t>(w.n_blocks) * w.h_count;
+      begin += static_cast<int64_t>(w.n_blocks) * (pair ? w.h_count / 2 : w.h_count);
       if (begin > 0x7fffffffLL) return false;
       group.push_back(w);
     }
@@ -527,6 +534,7 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   AttnParams base{};
   base.Hq = static_cast<int32_t>(Hq);
   base.group = static_cast<int32_t>(Hq / Hkv);
+  base.pair_heads = pair_heads(Hq, Hkv) ? 1 : 0;
   base.causal = causal ? 1 : 0;
   base.window = static_cast<int32_t>(window);
   base.q_pos_off = 0;
@@ -596,7 +604,7 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
       i = j;
     }
     if (items.empty()) continue;
-    if (!pack_items(items, causal, Hq, groups)) return SLOPE_ERR_UNSUPPORTED;
+    if (!pack_items(items, causal, Hq, base.pair_heads != 0, groups)) return SLOPE_ERR_UNSUPPORTED;
     for (const auto& g : groups)
       if ((st = run_attention(g, static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, to, base, tm, stream)) !=
           SLOPE_OK)
@@ -799,11 +807,12 @@ slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, co
     if (trim(q_off, q_off + Sq, k0, k1, causal, window)) it.kv[it.n_kv++] = Range{k0 - kv_off, k1 - k0};
   }
   std::vector<std::vector<WorkItem>> groups;
-  if (!pack_items({it}, causal, Hq, groups)) return SLOPE_ERR_UNSUPPORTED;
+  if (!pack_items({it}, causal, Hq, pair_heads(Hq, Hkv), groups)) return SLOPE_ERR_UNSUPPORTED;
 
   AttnParams base{};
   base.Hq = static_cast<int32_t>(Hq);
   base.group = static_cast<int32_t>(Hq / Hkv);
+  base.pair_heads = pair_heads(Hq, Hkv) ? 1 : 0;
   base.causal = causal ? 1 : 0;
   base.window = static_cast<int32_t>(window);
   base.q_pos_off = static_cast<int32_t>(q_off);

@@ -75,6 +75,8 @@ struct K1Cfg {
   static constexpr int kVTileBytes = kVChunks * kChunkBytes;
   static constexpr int kSlotBytes = kKTileBytes > kVTileBytes ? kKTileBytes : kVTileBytes;
   // 128 KB of K/V slots: 8 of 16 KB at d = 64, 4 of 32 KB with a 128-column K or V tile, 2 of 48 KB at 192
+  // (measured on the causal 32K zigzag workload: a second Q buffer, which leaves room for only
+  // 6 slots at d = 64, cost 2.5%)
   static constexpr int kSlots = 131072 / kSlotBytes;
   static constexpr int kNumBars = 1 + 2 * kSlots + 6 * kQTiles + 1 + 4 * kQTiles;
   // epilogue staging: 32-row x 32-column fp32 boxes (4 KB each, 128-byte swizzle), two per
@@ -204,42 +206,58 @@ __device__ __forceinline__ bool has_steps(const WorkItem& it, const AttnParams& 
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
-// One unit of work: an item's 256-row block for one query head.
+// One unit of work: an item's block of query rows for one head unit, i.e. 256 rows of one
+// head (Q tile t = rows 128t..128t+127 of the block) or, with pair_heads, 128 rows of two
+// heads of one KV group (Q tile t = head h + t).  With a pair the two Q tiles see exactly
+// the same keys under the same masks, so they take the same steps and reach the end of the
+// work tile together; 256 rows of one head give the second Q tile one more (diagonal) step.
 struct Tile {
   WorkItem itm;
-  int blk, h, g;
+  int blk, h, g;  // row block, first head of the unit, KV head
   TileGeom geo;
 };
 
-// Work tile w -> (item, row block, head).  Consecutive w are the heads of one row
+// First row (within the item) and head of Q tile t of a work tile.
+__device__ __forceinline__ int tile_row0(const AttnParams& p, const Tile& T, int t) {
+  return p.pair_heads ? T.blk * kBlockM : T.blk * kRowsPerCta + t * kBlockM;
+}
+__device__ __forceinline__ int tile_head(const AttnParams& p, const Tile& T, int t) {
+  return p.pair_heads ? T.h + t : T.h;
+}
+
+// Work tile w -> (item, row block, head unit).  Consecutive w are the units of one row
 // block (K/V shared in L2 by a KV group); items come heaviest first and an item's
 // later (heavier under the causal mask) row blocks before its earlier ones.
 // `ii` carries the item index from the caller's previous work tile: a CTA visits its
 // tiles in increasing w, so the item index never decreases and the scan resumes there.
-// kGrouped: tiles run head group by head group (p.head_group heads each); otherwise every
-// head of an item is inner to its row blocks (p.head_group is then the item's h_count).
+// kGrouped: tiles run unit group by unit group (p.head_group units each); otherwise every
+// unit of an item is inner to its row blocks.
 template <bool kGrouped>
 __device__ __forceinline__ void decode_tile(const AttnParams& p, const WorkItem* items, int w, Tile& T, int& ii) {
-  while (ii < p.n_items - 1 && w >= items[ii].tile_begin + items[ii].n_blocks * items[ii].h_count) ++ii;
+  const int ushift = p.pair_heads;  // head units per item = h_count >> ushift
+  while (ii < p.n_items - 1 && w >= items[ii].tile_begin + items[ii].n_blocks * (items[ii].h_count >> ushift)) ++ii;
   T.itm = items[ii];
   const int local = w - T.itm.tile_begin;
+  int unit;
   if constexpr (kGrouped) {
     const int hg = p.head_group;
     const int per_group = T.itm.n_blocks * hg;
     const int grp = local / per_group;
     const int rem = local - grp * per_group;
     T.blk = T.itm.n_blocks - 1 - rem / hg;
-    T.h = T.itm.h_begin + grp * hg + rem % hg;
+    unit = grp * hg + rem % hg;
   } else {
-    const int hc = T.itm.h_count;
-    T.blk = T.itm.n_blocks - 1 - local / hc;
-    T.h = T.itm.h_begin + local % hc;
+    const int hu = T.itm.h_count >> ushift;
+    T.blk = T.itm.n_blocks - 1 - local / hu;
+    unit = local % hu;
   }
+  T.h = T.itm.h_begin + (unit << ushift);
   T.g = T.h / p.group;
 #pragma unroll
   for (int t = 0; t < kQTiles; ++t) {
-    T.geo.rows[t] = max(0, min(kBlockM, T.itm.q_len - T.blk * kRowsPerCta - t * kBlockM));
-    T.geo.qa[t] = p.q_pos_off + T.itm.q_row0 + T.blk * kRowsPerCta + t * kBlockM;
+    const int r0 = tile_row0(p, T, t);
+    T.geo.rows[t] = max(0, min(kBlockM, T.itm.q_len - r0));
+    T.geo.qa[t] = p.q_pos_off + T.itm.q_row0 + r0;
     T.geo.qb[t] = T.geo.qa[t] + T.geo.rows[t] - 1;
   }
 }
@@ -340,8 +358,8 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         mbar_arrive_expect_tx(bar_q, nq * C::kQTileBytes);
         for (int t = 0; t < nq; ++t)
           for (int c = 0; c < C::kQChunks; ++c)
-            tma_load_3d(sQ + t * C::kQTileBytes + c * kChunkBytes, &tm_q, bar_q, 64 * c, T.h,
-                        T.itm.q_row0 + T.blk * kRowsPerCta + t * kBlockM);
+            tma_load_3d(sQ + t * C::kQTileBytes + c * kChunkBytes, &tm_q, bar_q, 64 * c, tile_head(p, T, t),
+                        T.itm.q_row0 + tile_row0(p, T, t));
         ++wt;  // Q loads issued
         ok = for_each_step(T.itm, p, T.geo, [&](const Step& s) -> bool {
           {  // K tile
@@ -732,9 +750,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       if (nl > 0) ok = warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 10));
       if (!ok) break;
       const bool valid_row = row < rows_t;
-      const int64_t orow = static_cast<int64_t>(T.itm.out_row0) + T.blk * kRowsPerCta + t * kBlockM + row;
+      const int64_t orow = static_cast<int64_t>(T.itm.out_row0) + tile_row0(p, T, t) + row;
+      const int head = tile_head(p, T, t);
       float* op = p.out + static_cast<int64_t>(T.itm.plane) * p.out_splane + orow * p.out_srow +
-                  static_cast<int64_t>(T.h) * p.out_shead;
+                  static_cast<int64_t>(head) * p.out_shead;
       // A warp whose 32 rows are all valid writes O through shared memory and TMA stores
       // (one 32 x 32 box per 32 columns): each thread's row lies a whole output row apart
       // from its neighbour's, so direct stores would touch 32 cache lines per instruction.
@@ -748,7 +767,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           // bf16 output: two 32-column TMEM loads fill one 64-column (128-byte) box row
           __nv_bfloat16* bp = reinterpret_cast<__nv_bfloat16*>(p.out) +
                               (static_cast<int64_t>(T.itm.plane) * p.out_splane + orow * p.out_srow +
-                               static_cast<int64_t>(T.h) * p.out_shead);
+                               static_cast<int64_t>(head) * p.out_shead);
 #pragma unroll
           for (int g = 0; g < DV / 64; ++g) {
             uint32_t wv[32];
@@ -785,7 +804,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
               __syncwarp();
               if (lane == 0) {
                 const int64_t z = static_cast<int64_t>(T.itm.plane) * p.out_plane_rows + orow;  // row of lane 0
-                tma_store_3d(&tm_o, box, 64 * g, T.h, static_cast<int>(z));
+                tma_store_3d(&tm_o, box, 64 * g, head, static_cast<int>(z));
                 bulk_commit();
               }
             } else if (valid_row) {
@@ -829,7 +848,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
               __syncwarp();
               if (lane == 0) {
                 const int64_t z = static_cast<int64_t>(T.itm.plane) * p.out_plane_rows + orow;  // row of lane 0
-                tma_store_3d(&tm_o, box, 32 * c, T.h, static_cast<int>(z));
+                tma_store_3d(&tm_o, box, 32 * c, head, static_cast<int>(z));
                 bulk_commit();
               }
             } else if (valid_row) {
@@ -846,7 +865,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         if (p.out_bf16) {
           __nv_bfloat16* bp = reinterpret_cast<__nv_bfloat16*>(p.out) +
                               (static_cast<int64_t>(T.itm.plane) * p.out_splane + orow * p.out_srow +
-                               static_cast<int64_t>(T.h) * p.out_shead);
+                               static_cast<int64_t>(head) * p.out_shead);
 #pragma unroll
           for (int i = 0; i < DV / 8; ++i) *reinterpret_cast<uint4*>(bp + 8 * i) = make_uint4(0u, 0u, 0u, 0u);
         } else {
@@ -856,7 +875,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       }
       if (valid_row) {
         p.lse[static_cast<int64_t>(T.itm.plane) * p.lse_splane + orow * p.lse_srow +
-              static_cast<int64_t>(T.h) * p.lse_shead] = l > 0.f ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
+              static_cast<int64_t>(head) * p.lse_shead] = l > 0.f ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
       }
     }
     // the O stores of this warp complete before the CTA releases its shared memory
@@ -891,17 +910,17 @@ int gcd_int(int a, int b) {
   return a;
 }
 
-// Query heads per tile group.  With every head of an item inner to its row blocks, the
-// resident CTAs work on about grid / heads row blocks at a time.  When a KV head serves few
-// query heads (Hq / Hkv < 4, as in MLA-shaped attention), that is about one CTA per KV head,
-// so each CTA streams its own K/V tiles from DRAM.  A group of heads just large enough to
-// give the grid one group's row blocks puts many CTAs on the same heads, and they then share
-// those heads' K/V tiles in L2.  With larger GQA groups the query heads of a KV head already
-// share its tiles, and one group of all the heads is kept.
+// Head units (heads, or head pairs with pair_heads) per tile group.  With every unit of an
+// item inner to its row blocks, the resident CTAs work on about grid / units row blocks at a
+// time.  When a KV head serves few query heads (Hq / Hkv < 4, as in MLA-shaped attention),
+// that is about one CTA per KV head, so each CTA streams its own K/V tiles from DRAM.  A group
+// of units just large enough to give the grid one group's row blocks puts many CTAs on the
+// same heads, and they then share those heads' K/V tiles in L2.  With larger GQA groups the
+// query heads of a KV head already share its tiles, and one group of all the units is kept.
 int tile_head_group(const AttnParams& p, long long grid) {
   int common = 0, max_blocks = 1;
   for (int i = 0; i < p.n_items; ++i) {
-    common = gcd_int(common, p.items[i].h_count);
+    common = gcd_int(common, p.items[i].h_count >> p.pair_heads);
     max_blocks = std::max(max_blocks, static_cast<int>(p.items[i].n_blocks));
   }
   if (common <= 0) return 1;
@@ -918,7 +937,8 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   using C = K1Cfg<DQK, DV>;
   if (p.n_items <= 0) return cudaSuccess;
   const WorkItem& last = p.items[p.n_items - 1];
-  const long long tiles = static_cast<long long>(last.tile_begin) + static_cast<long long>(last.n_blocks) * last.h_count;
+  const long long tiles =
+      static_cast<long long>(last.tile_begin) + static_cast<long long>(last.n_blocks) * (last.h_count >> p.pair_heads);
   if (tiles <= 0) return cudaSuccess;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   p.total_tiles = static_cast<int32_t>(tiles);

@@ -23,17 +23,19 @@ struct KvRange {
 };
 
 // One query block of a range of query heads, and the key/value ranges it attends to in
-// this launch.  Its work tiles are (row block, head) pairs: head group by head group
-// (AttnParams::head_group heads each), and in a group row blocks from the last one down
-// with the group's heads inner.
+// this launch.  Its work tiles are (row block, head unit) pairs, where a head unit is one
+// head (the CTA's two Q tiles are 256 consecutive rows of it) or, with
+// AttnParams::pair_heads, two heads of one KV group (the two Q tiles are the same 128
+// rows of both).  Tiles run unit group by unit group (AttnParams::head_group units each),
+// and in a group row blocks from the last one down with the group's units inner.
 struct WorkItem {
   int32_t q_row0;      // first query row (in q)
   int32_t q_len;       // query rows
   int32_t out_row0;    // output row of q_row0
   int32_t plane;       // output plane
   int32_t n_kv;        // 0..kMaxKvRanges
-  int32_t tile_begin;  // first work tile of this item (prefix sum over items of n_blocks * h_count)
-  int32_t n_blocks;    // ceil(q_len / kRowsPerCta)
+  int32_t tile_begin;  // first work tile of this item (prefix sum over items of n_blocks * head units)
+  int32_t n_blocks;    // ceil(q_len / rows per work tile): 128 with pair_heads, else kRowsPerCta
   int32_t h_begin;     // first query head
   int32_t h_count;     // query heads (whole KV-head groups)
   KvRange kv[kMaxKvRanges];
@@ -43,8 +45,10 @@ static_assert(sizeof(WorkItem) % 4 == 0, "work items are copied as 32-bit words"
 struct AttnParams {
   int32_t n_items;
   int32_t total_tiles;      // work tiles (sum over items of row blocks x heads); set by the launcher
-  int32_t head_group;       // query heads per tile group (divides every item's h_count; 0 = one group per
-                            // item); set by the launcher
+  int32_t head_group;       // head units per tile group (divides every item's unit count; 0 = one group
+                            // per item); set by the launcher
+  int32_t pair_heads;       // 1: a work tile's two Q tiles are two heads of one KV group on the same
+                            // 128 rows (needs an even Hq / Hkv); 0: 256 consecutive rows of one head
   int32_t Hq;
   int32_t group;            // Hq / Hkv
   int32_t causal;
