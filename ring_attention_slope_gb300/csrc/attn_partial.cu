@@ -731,9 +731,12 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         ++nl;
         return true;
       };
-      for (int r = 0; r < T.itm.n_kv && ok; ++r) {
-        const TileRange R = tile_range(r == 0 ? T.itm.kv[0].row0 : T.itm.kv[1].row0,
-                                       r == 0 ? T.itm.kv[0].len : T.itm.kv[1].len, qa_t, qb_t, p);
+      // the item's fields are read from shared memory where they are used, rather than kept in
+      // registers across the steps, which need every register they can get
+      const WorkItem& sit = sItems[item_hint];
+      for (int r = 0; r < sit.n_kv && ok; ++r) {
+        const KvRange kr = sit.kv[r];
+        const TileRange R = tile_range(kr.row0, kr.len, qa_t, qb_t, p);
         for (int j = R.lo; j <= R.hi && ok; ++j)
           ok = step(j >= R.flo && j <= R.fhi, R.kpos0 + j * kBlockN, min(kBlockN, R.len - j * kBlockN));
       }
@@ -747,27 +750,32 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       if (!ok) break;
 
       // ---- epilogue: out = O / l, lse = ln(sum exp(scaled scores))
+      // What does not depend on O (the row's 1/l, its lse, the output address) is done before
+      // the wait for the tile's last PV.
+      const bool valid_row = row < rows_t;
+      const int head = tile_head(p, T, t);
+      const int64_t orow = static_cast<int64_t>(sit.out_row0) + tile_row0(p, T, t) + row;
+      const int64_t plane = sit.plane;
+      if (valid_row) {
+        p.lse[plane * p.lse_splane + orow * p.lse_srow + static_cast<int64_t>(head) * p.lse_shead] =
+            l > 0.f ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
+      }
+      // a row that saw no key keeps m = -inf; its l holds only the clamped 2^-125
+      // terms of the polynomial pairs, and its output is 0
+      const float inv = (l > 0.f && m_used > -INFINITY) ? 1.f / l : 0.f;
+      float* op = p.out + plane * p.out_splane + orow * p.out_srow + static_cast<int64_t>(head) * p.out_shead;
       if (nl > 0) ok = warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 10));
       if (!ok) break;
-      const bool valid_row = row < rows_t;
-      const int64_t orow = static_cast<int64_t>(T.itm.out_row0) + tile_row0(p, T, t) + row;
-      const int head = tile_head(p, T, t);
-      float* op = p.out + static_cast<int64_t>(T.itm.plane) * p.out_splane + orow * p.out_srow +
-                  static_cast<int64_t>(head) * p.out_shead;
       // A warp whose 32 rows are all valid writes O through shared memory and TMA stores
       // (one 32 x 32 box per 32 columns): each thread's row lies a whole output row apart
       // from its neighbour's, so direct stores would touch 32 cache lines per instruction.
       const bool via_tma = p.out_tma && __all_sync(0xffffffffu, valid_row);
       if (nl > 0) {
         tc_fence_after_sync();
-        // a row that saw no key keeps m = -inf; its l holds only the clamped 2^-125
-        // terms of the polynomial pairs, and its output is 0
-        const float inv = (l > 0.f && m_used > -INFINITY) ? 1.f / l : 0.f;
         if (p.out_bf16) {
           // bf16 output: two 32-column TMEM loads fill one 64-column (128-byte) box row
           __nv_bfloat16* bp = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                              (static_cast<int64_t>(T.itm.plane) * p.out_splane + orow * p.out_srow +
-                               static_cast<int64_t>(head) * p.out_shead);
+                              (plane * p.out_splane + orow * p.out_srow + static_cast<int64_t>(head) * p.out_shead);
 #pragma unroll
           for (int g = 0; g < DV / 64; ++g) {
             uint32_t wv[32];
@@ -803,7 +811,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
               fence_proxy_async_shared();
               __syncwarp();
               if (lane == 0) {
-                const int64_t z = static_cast<int64_t>(T.itm.plane) * p.out_plane_rows + orow;  // row of lane 0
+                const int64_t z = plane * p.out_plane_rows + orow;  // row of lane 0
                 tma_store_3d(&tm_o, box, 64 * g, head, static_cast<int>(z));
                 bulk_commit();
               }
@@ -847,7 +855,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
               fence_proxy_async_shared();
               __syncwarp();
               if (lane == 0) {
-                const int64_t z = static_cast<int64_t>(T.itm.plane) * p.out_plane_rows + orow;  // row of lane 0
+                const int64_t z = plane * p.out_plane_rows + orow;  // row of lane 0
                 tma_store_3d(&tm_o, box, 32 * c, head, static_cast<int>(z));
                 bulk_commit();
               }
@@ -864,18 +872,13 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       } else if (p.write_empty_out && valid_row) {
         if (p.out_bf16) {
           __nv_bfloat16* bp = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                              (static_cast<int64_t>(T.itm.plane) * p.out_splane + orow * p.out_srow +
-                               static_cast<int64_t>(head) * p.out_shead);
+                              (plane * p.out_splane + orow * p.out_srow + static_cast<int64_t>(head) * p.out_shead);
 #pragma unroll
           for (int i = 0; i < DV / 8; ++i) *reinterpret_cast<uint4*>(bp + 8 * i) = make_uint4(0u, 0u, 0u, 0u);
         } else {
 #pragma unroll
           for (int i = 0; i < DV / 4; ++i) *reinterpret_cast<float4*>(op + 4 * i) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-      }
-      if (valid_row) {
-        p.lse[static_cast<int64_t>(T.itm.plane) * p.lse_splane + orow * p.lse_srow +
-              static_cast<int64_t>(head) * p.lse_shead] = l > 0.f ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
       }
     }
     // the O stores of this warp complete before the CTA releases its shared memory
