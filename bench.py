@@ -296,6 +296,27 @@ def measure_job(ctx, w, window, q, k, v, steps, warmup, flags=()):
     if st != 0:
         raise RuntimeError(f"device status {st} at site {site}")
 
+    # ---- the job: `steps` plain calls between two events (consecutive attention launches of a call
+    # overlap their tails, which per-launch events would prevent)
+    sampler = ClockSampler(ctx.local)
+    sampler.start()
+    time.sleep(0.15)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ctx.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for _ in range(steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    ctx.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), ctx.dist, "cuda")
+    st, site = slope.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} at site {site}")
+
+    # ---- each kernel's own duration: the same steps again with CUDA events around every launch
     n_pairs = launches_per_step + 8
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_pairs)]
           for _ in range(steps)]
@@ -304,24 +325,13 @@ def measure_job(ctx, w, window, q, k, v, steps, warmup, flags=()):
             a.record(stream)
             b.record(stream)
     torch.cuda.synchronize()
-    sampler = ClockSampler(ctx.local)
-    sampler.start()
-    time.sleep(0.15)
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     kinds_all, counts = [], []
-    ctx.barrier()
-    torch.cuda.synchronize()
-    t_start.record(stream)
     for s in range(steps):
         _, _, nl, kinds = slope.cp_prefill_timed(q, k, v, n, w.layout, ev[s], chunk_sizes=sizes, window=window,
                                                  out=out, lse=lse, workspace=ws)
         counts.append(nl)
         kinds_all.append(kinds)
-    t_end.record(stream)
     torch.cuda.synchronize()
-    ctx.barrier()
-    clocks = sampler.stop()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), ctx.dist, "cuda")
     st, site = slope.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} at site {site}")
@@ -356,6 +366,8 @@ def measure_job(ctx, w, window, q, k, v, steps, warmup, flags=()):
                            "avg_launch_ms": k2_ms / max(1, k2_n)},
         "gpu_launches": int(sum(counts)),
         "clocks": clocks,
+        "timing": "value: steps x slope_cp_prefill between two CUDA events; kernel durations: a second pass of "
+                  "the same steps through slope_cp_prefill_timed (events around every launch)",
         "config": {"workload": w.name, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "dqk": w.dqk, "dv": w.dv,
                    "layout": w.layout, "n_chunks": n, "window": window, "batch": 1,
                    "l2": f"inputs larger than L2 (Q+K+V {q.numel() * 2 + k.numel() * 2 + v.numel() * 2} B, "

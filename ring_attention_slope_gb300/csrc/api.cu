@@ -441,14 +441,17 @@ cudaError_t record(Timing* tm, bool before, int kind, cudaStream_t stream) {
   return e;
 }
 
+// dependent: this launch follows another attention launch of the same call in the stream (see
+// launch_attn_partial); never the first launch of a call, which may follow a kernel that reads
+// what this one writes.  Launches timed with events run the ordinary way.
 slope_status run_attention(const std::vector<WorkItem>& group, int dqk, int dv, const CUtensorMap& tq,
                            const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to, AttnParams base,
-                           Timing* tm, cudaStream_t stream) {
+                           bool dependent, Timing* tm, cudaStream_t stream) {
   base.n_items = static_cast<int32_t>(group.size());
   for (size_t i = 0; i < group.size(); ++i) base.items[i] = group[i];
   cudaError_t e;
   if ((e = record(tm, true, 0, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
-  if ((e = launch_attn_partial(dqk, dv, tq, tk, tv, to, base, stream)) != cudaSuccess)
+  if ((e = launch_attn_partial(dqk, dv, tq, tk, tv, to, base, dependent && tm == nullptr, stream)) != cudaSuccess)
     return cuda_fail("attention kernel launch", e);
   if ((e = record(tm, false, 0, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
   return SLOPE_OK;
@@ -591,6 +594,7 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   // a kernel launch up to the launch's item limit: each partial is computed by the same code
   // as in a launch of its own, with fewer launch prologues and tails.
   size_t i = 0;
+  int launched = 0;  // attention launches of this call so far
   std::vector<std::vector<WorkItem>> groups;
   for (int l = 0; l < plan.n_launches;) {
     std::vector<PItem> items;
@@ -605,10 +609,12 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
     }
     if (items.empty()) continue;
     if (!pack_items(items, causal, Hq, base.pair_heads != 0, groups)) return SLOPE_ERR_UNSUPPORTED;
-    for (const auto& g : groups)
-      if ((st = run_attention(g, static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, to, base, tm, stream)) !=
-          SLOPE_OK)
+    for (const auto& g : groups) {
+      if ((st = run_attention(g, static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, to, base, launched > 0, tm,
+                              stream)) != SLOPE_OK)
         return st;
+      ++launched;
+    }
   }
   if (plan.direct) return SLOPE_OK;
 
@@ -834,7 +840,7 @@ slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, co
   base.out_bf16 = out->dtype == SLOPE_BF16 ? 1 : 0;
   base.out_tma = make_out_map(&to, out->data, base.out_bf16 != 0, Sq, Hq, dv, out->stride[0], out->stride[1]) ? 1 : 0;
   if (!base.out_tma) to = tq;  // never used
-  return run_attention(groups[0], static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, to, base, nullptr,
+  return run_attention(groups[0], static_cast<int>(dqk), static_cast<int>(dv), tq, tk, tv, to, base, false, nullptr,
                        static_cast<cudaStream_t>(stream));
 }
 

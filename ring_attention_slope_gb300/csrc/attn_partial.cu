@@ -290,10 +290,18 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = p.total_tiles;
 
+  // The next attention launch of a decomposition (independent of this one: it reads the same
+  // inputs and writes other partial planes) may take each SM this grid leaves, as soon as
+  // every CTA of this grid has started.
+  pdl_launch_dependents();
+
   // ---- a CTA scheduled after a timeout elsewhere does nothing
   if (threadIdx.x == 0) *cta_abort = (*reinterpret_cast<volatile int*>(p.status) != 0) ? 1 : 0;
   __syncthreads();
-  if (*cta_abort) return;
+  if (*cta_abort) {
+    pdl_wait();
+    return;
+  }
 
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
@@ -892,6 +900,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
   }
+  // Launched as a dependent of the previous attention launch, this grid finishes only after
+  // that one has: a kernel queued after the last launch (the merge) then sees every launch's
+  // partials.
+  pdl_wait();
 }
 
 // CTAs per launch: one persistent CTA per SM (each holds the SM's whole TMEM),
@@ -936,7 +948,7 @@ int tile_head_group(const AttnParams& p, long long grid) {
 
 template <int DQK, int DV>
 cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-                        AttnParams p, cudaStream_t stream) {
+                        AttnParams p, bool dependent, cudaStream_t stream) {
   using C = K1Cfg<DQK, DV>;
   if (p.n_items <= 0) return cudaSuccess;
   const WorkItem& last = p.items[p.n_items - 1];
@@ -950,8 +962,17 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_partial_kernel<DQK, DV><<<static_cast<unsigned>(grid), kK1Threads, C::kSmemBytes, stream>>>(tq, tk, tv, to, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kK1Threads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_partial_kernel<DQK, DV>, tq, tk, tv, to, p);
 }
 
 }  // namespace
@@ -964,13 +985,13 @@ bool attn_partial_supported(int dqk, int dv) {
 }
 
 cudaError_t launch_attn_partial(int dqk, int dv, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& to, const AttnParams& p, cudaStream_t stream) {
-  if (dqk == 64 && dv == 64) return launch_impl<64, 64>(tq, tk, tv, to, p, stream);
-  if (dqk == 64 && dv == 128) return launch_impl<64, 128>(tq, tk, tv, to, p, stream);
-  if (dqk == 128 && dv == 64) return launch_impl<128, 64>(tq, tk, tv, to, p, stream);
-  if (dqk == 128 && dv == 128) return launch_impl<128, 128>(tq, tk, tv, to, p, stream);
-  if (dqk == 192 && dv == 64) return launch_impl<192, 64>(tq, tk, tv, to, p, stream);
-  if (dqk == 192 && dv == 128) return launch_impl<192, 128>(tq, tk, tv, to, p, stream);
+                                const CUtensorMap& to, const AttnParams& p, bool dependent, cudaStream_t stream) {
+  if (dqk == 64 && dv == 64) return launch_impl<64, 64>(tq, tk, tv, to, p, dependent, stream);
+  if (dqk == 64 && dv == 128) return launch_impl<64, 128>(tq, tk, tv, to, p, dependent, stream);
+  if (dqk == 128 && dv == 64) return launch_impl<128, 64>(tq, tk, tv, to, p, dependent, stream);
+  if (dqk == 128 && dv == 128) return launch_impl<128, 128>(tq, tk, tv, to, p, dependent, stream);
+  if (dqk == 192 && dv == 64) return launch_impl<192, 64>(tq, tk, tv, to, p, dependent, stream);
+  if (dqk == 192 && dv == 128) return launch_impl<192, 128>(tq, tk, tv, to, p, dependent, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -95,8 +95,11 @@ struct MergeParams {
 constexpr int kStatusTimeout = 1;
 
 // Host-side launchers (defined in attn_partial.cu / lse_merge.cu / status.cu).
+// dependent: launch as a programmatic dependent of the previous kernel in the stream, which
+// must be another attention launch of the same decomposition (one that writes none of what
+// this one reads or writes).
 cudaError_t launch_attn_partial(int dqk, int dv, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, const CUtensorMap& to, const AttnParams& p,
+                                const CUtensorMap& tv, const CUtensorMap& to, const AttnParams& p, bool dependent,
                                 cudaStream_t stream);
 bool attn_partial_supported(int dqk, int dv);
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);

@@ -75,6 +75,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
+// ----------------------------------------------------------------- programmatic dependent launch
+
+// Lets the next kernel of the stream, when it is launched as a programmatic dependent, be
+// scheduled as soon as every CTA of this grid has executed this (or exited).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grid this one was launched as a programmatic dependent of has completed and
+// its memory writes are visible; returns at once for a kernel launched the ordinary way.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
