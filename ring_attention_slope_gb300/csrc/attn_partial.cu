@@ -772,12 +772,12 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       // terms of the polynomial pairs, and its output is 0
       const float inv = (l > 0.f && m_used > -INFINITY) ? 1.f / l : 0.f;
       float* op = p.out + plane * p.out_splane + orow * p.out_srow + static_cast<int64_t>(head) * p.out_shead;
-      if (nl > 0) ok = warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 10));
-      if (!ok) break;
       // A warp whose 32 rows are all valid writes O through shared memory and TMA stores
       // (one 32 x 32 box per 32 columns): each thread's row lies a whole output row apart
       // from its neighbour's, so direct stores would touch 32 cache lines per instruction.
       const bool via_tma = p.out_tma && __all_sync(0xffffffffu, valid_row);
+      if (nl > 0) ok = warp_all(wait_bounded(&bar_o[t], (n - 1) & 1, cta_abort, p.status, limit, 10));
+      if (!ok) break;
       if (nl > 0) {
         tc_fence_after_sync();
         if (p.out_bf16) {
@@ -831,48 +831,59 @@ __global__ void __launch_bounds__(kK1Threads, 1)
             }
           }
         } else {
+          // fp32 output, as many 32-column chunks at a time as there are staging boxes: each is
+          // loaded from TMEM and written to its box in turn, and the group's boxes then share one
+          // proxy fence and one bulk group of TMA stores
+          constexpr int kG = C::kStageBufs;
+          static_assert((DV / 32) % kG == 0, "whole groups of chunks");
 #pragma unroll
-          for (int c = 0; c < DV / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait();
-            reg_fence(o);
-            if (c == DV / 32 - 1) {  // O_t is read: the next work tile's first PV may overwrite it
-              tc_fence_before_sync();
+          for (int c0 = 0; c0 < DV / 32; c0 += kG) {
+            if (via_tma) {
+              // the stores that last used these boxes have read them
+              if (lane == 0) bulk_wait_read_all();
               __syncwarp();
-              if (lane == 0) mbar_arrive(&bar_ofree[t]);
+            }
+#pragma unroll
+            for (int b = 0; b < kG; ++b) {
+              const int c = c0 + b;
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_ld_wait();
+              reg_fence(o);
+              if (c == DV / 32 - 1) {  // O_t is read: the next work tile's first PV may overwrite it
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_ofree[t]);
+              }
+              if (via_tma) {
+                // row `lane` of the box: 16-byte chunk i at chunk position i ^ (lane & 7) (128-byte swizzle)
+                uint8_t* const box = sStage + b * 4096;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                               __uint_as_float(o[4 * i + 2]) * inv,
+                                               __uint_as_float(o[4 * i + 3]) * inv);
+                  *reinterpret_cast<float4*>(box + lane * 128 + ((i ^ (lane & 7)) * 16)) = v;
+                }
+              } else if (valid_row) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                               __uint_as_float(o[4 * i + 2]) * inv,
+                                               __uint_as_float(o[4 * i + 3]) * inv);
+                  *reinterpret_cast<float4*>(op + c * 32 + 4 * i) = v;
+                }
+              }
             }
             if (via_tma) {
-              uint8_t* const box = sStage + (c % C::kStageBufs) * 4096;
-              // the store that last used this box has read it (with two boxes the most
-              // recent store, into the other box, may still be reading)
-              if (lane == 0) {
-                if (C::kStageBufs == 2)
-                  bulk_wait_read_allbut1();
-                else
-                  bulk_wait_read_all();
-              }
-              __syncwarp();
-              // row `lane` of the box: 16-byte chunk i at chunk position i ^ (lane & 7) (128-byte swizzle)
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                             __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-                *reinterpret_cast<float4*>(box + lane * 128 + ((i ^ (lane & 7)) * 16)) = v;
-              }
               fence_proxy_async_shared();
               __syncwarp();
               if (lane == 0) {
                 const int64_t z = plane * p.out_plane_rows + orow;  // row of lane 0
-                tma_store_3d(&tm_o, box, 32 * c, head, static_cast<int>(z));
-                bulk_commit();
-              }
-            } else if (valid_row) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                       __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-                *reinterpret_cast<float4*>(op + c * 32 + 4 * i) = v;
+                for (int b = 0; b < kG; ++b)
+                  tma_store_3d(&tm_o, sStage + b * 4096, 32 * (c0 + b), head, static_cast<int>(z));
+                bulk_commit();
               }
             }
           }
