@@ -336,17 +336,20 @@ def measure_job(ctx, w, window, q, k, v, steps, warmup, flags=()):
     if st != 0:
         raise RuntimeError(f"device status {st} at site {site}")
 
-    k1_ms, k2_ms, k1_n, k2_n = 0.0, 0.0, 0, 0
+    k1_ms, k2_ms, kf_ms, k1_n, k2_n, kf_n = 0.0, 0.0, 0.0, 0, 0, 0
     for s in range(steps):
         for i in range(counts[s]):
             a, b = ev[s][i]
             d = a.elapsed_time(b)
-            if kinds_all[s][i] == 0:
+            if kinds_all[s][i] == 0:  # attention
                 k1_ms += d
                 k1_n += 1
-            else:
+            elif kinds_all[s][i] == 1:  # merge
                 k2_ms += d
                 k2_n += 1
+            else:  # the -inf fill of the live partial lse planes
+                kf_ms += d
+                kf_n += 1
     flops_step = workload_flops(w, window)
     merge_bytes = merge_bytes_per_launch(slope, w, n, sizes, window)
     k2_gbs = merge_bytes * k2_n / (k2_ms * 1e-3) / 1e9 if k2_ms > 0 else None
@@ -363,7 +366,10 @@ def measure_job(ctx, w, window, q, k, v, steps, warmup, flags=()):
                            "frac": (k2_gbs / peaks["hbm_gbs"]) if k2_gbs else None,
                            "peak_source": f"{ctx.peak_src} hbm_gbs",
                            "bytes_per_launch": merge_bytes, "kernel": "lse_merge_kernel",
-                           "avg_launch_ms": k2_ms / max(1, k2_n)},
+                           "avg_launch_ms": k2_ms / max(1, k2_n),
+                           "lse_fill": {"kernel": "lse_fill_kernel", "launches": kf_n,
+                                        "avg_launch_ms": kf_ms / max(1, kf_n),
+                                        "bytes_per_launch": fill_bytes_per_launch(slope, w, n, sizes, window)}},
         "gpu_launches": int(sum(counts)),
         "clocks": clocks,
         "timing": "value: steps x slope_cp_prefill between two CUDA events; kernel durations: a second pass of "
@@ -541,6 +547,13 @@ def merge_bytes_per_launch(slope, w, n, sizes, window):
         live_rows[it["plane"]] += int(seen.sum())
     reads = int(plane_live.sum()) * w.S * 4 + int(live_rows[plane_live].sum()) * w.dv * 4
     return float(w.Hq * (reads + w.S * (w.dv * 2 + 4)))
+
+
+def fill_bytes_per_launch(slope, w, n, sizes, window):
+    """Bytes the lse fill writes per call: -inf into every live partial plane's lse ([S, Hq] fp32)."""
+    items, _, n_planes = slope.cp_prefill_plan(w.S, n, w.layout, chunk_sizes=sizes, causal=True, window=window)
+    live = {0} | {it["plane"] for it in items if it["kv"]}
+    return float(len(live) * w.S * w.Hq * 4)
 
 
 def launch_groups(items, n_launch):

@@ -333,7 +333,9 @@ SLOPE_API slope_status slope_cp_prefill_host(const slope_tensor* q_host, const s
  * i and events[2*i+1] after it.  events is a host array of 2*n_event_pairs
  * cudaEvent_t handles created by the caller.  On return *n_launches holds the
  * number of launches made and launch_kind[i] (if non-NULL, n_event_pairs
- * entries) is 0 for an attention-partial launch and 1 for the merge.
+ * entries) is 0 for an attention-partial launch, 1 for the merge and 2 for
+ * the fill that sets the live partial planes' lse to -inf before the
+ * attention launches.
  * Returns SLOPE_ERR_SHAPE if n_event_pairs is smaller than the launch count.
  */
 SLOPE_API slope_status slope_cp_prefill_timed(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v,
@@ -346,9 +348,13 @@ SLOPE_API slope_status slope_cp_prefill_timed(const slope_tensor* q, const slope
  * Host-only view of the work decomposition slope_cp_prefill performs (no GPU
  * needed).  One entry per (launch, query block): the query rows, the partial
  * plane written and the key/value row ranges attended in that launch
- * (after dropping blocks the mask hides entirely).  An entry with n_kv = 0
- * stands for rows whose partial is empty; a plane whose entries all have
- * n_kv = 0 is neither launched nor merged (plane 0 always is).
+ * (after dropping blocks the mask hides entirely).  In the ring and chunked
+ * layouts an entry keeps only the query rows that see at least one of its
+ * keys, and a block none of whose rows sees a key has no entry: the call first
+ * sets the lse of every live partial plane to -inf, so rows in no entry of a
+ * plane are empty partials the merge skips.  A plane with no entry is neither
+ * launched nor merged (plane 0 always is).  Ulysses and fused entries cover
+ * every row (they write the final output).
  */
 typedef struct {
   int32_t launch;     /* attention launch index (ring step or chunk)      */

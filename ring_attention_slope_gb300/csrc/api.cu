@@ -340,6 +340,41 @@ slope_status build_base_plan(int64_t S, int n_chunks, slope_layout layout, const
   return SLOPE_ERR_LAYOUT;
 }
 
+// Partial plans: each item keeps only the query rows that see at least one of its keys (the
+// hull of those rows over its key ranges, with the ranges trimmed again to them), and an item
+// whose rows see none is dropped.  Rows left out of every item of a plane keep the -inf lse
+// that the call writes into the partial planes before the attention launches, so the merge
+// skips them without the attention kernel visiting them.  Positions are row indices here.
+void keep_rows_that_see_keys(Plan& plan, int causal, int64_t window) {
+  std::vector<PItem> kept;
+  kept.reserve(plan.items.size());
+  for (const PItem& it : plan.items) {
+    const int64_t q0 = it.q_row0, q1 = it.q_row0 + it.q_len;
+    int64_t lo = q1, hi = q0 - 1;  // hull of the live rows
+    for (int r = 0; r < it.n_kv; ++r) {
+      const int64_t k0 = it.kv[r].row0, k1 = k0 + it.kv[r].len;
+      // row i sees a key of [k0, k1) iff (!causal || i >= k0) && (window == 0 || i - window + 1 <= k1 - 1)
+      const int64_t a = causal ? std::max(q0, k0) : q0;
+      const int64_t b = window > 0 ? std::min(q1 - 1, k1 + window - 2) : q1 - 1;
+      if (a <= b) {
+        lo = std::min(lo, a);
+        hi = std::max(hi, b);
+      }
+    }
+    if (lo > hi) continue;
+    PItem t = it;
+    t.q_row0 = lo;
+    t.q_len = hi - lo + 1;
+    t.n_kv = 0;
+    for (int r = 0; r < it.n_kv; ++r) {
+      int64_t k0 = it.kv[r].row0, k1 = k0 + it.kv[r].len;
+      if (trim(lo, hi + 1, k0, k1, causal, window)) t.kv[t.n_kv++] = Range{k0, k1 - k0};
+    }
+    kept.push_back(t);
+  }
+  plan.items = std::move(kept);
+}
+
 // The layout word: the base layout in the low 8 bits and, for the ring and chunked layouts, a
 // Ulysses degree u in bits 8-15 (0 or 1: none).  Ulysses x Ring: each of the base plan's items
 // is split into u items, one per query-head group (the ranks of one Ulysses group after the
@@ -352,6 +387,7 @@ slope_status build_plan(int64_t S, int n_chunks, slope_layout layout, const int6
   const int u = static_cast<int>((word >> 8) & 0xffu);
   slope_status st =
       build_base_plan(S, n_chunks, base, chunk_sizes, causal, window, (flags & SLOPE_CP_FUSED) != 0, plan);
+  if (st == SLOPE_OK && !plan.direct) keep_rows_that_see_keys(plan, causal, window);
   if (st != SLOPE_OK || u <= 1) return st;
   if (base == SLOPE_LAYOUT_ULYSSES || u > kMaxRanks) {
     plan = Plan();
@@ -588,6 +624,18 @@ slope_status cp_prefill_impl(const slope_tensor* q, const slope_tensor* k, const
   plane_live[0] = 1;
   for (const PItem& it : plan.items)
     if (it.n_kv > 0) plane_live[static_cast<size_t>(it.plane)] = 1;
+  if (!plan.direct) {
+    // the live planes' lse starts at -inf: rows that no item covers read as empty partials
+    FillParams fp{};
+    fp.base = lse_planes;
+    fp.plane_elems = S * Hq;
+    for (int pl = 0; pl < plan.n_planes; ++pl)
+      if (plane_live[static_cast<size_t>(pl)]) fp.planes[fp.n++] = pl;
+    cudaError_t e;
+    if ((e = record(tm, true, 2, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
+    if ((e = launch_lse_fill(fp, stream)) != cudaSuccess) return cuda_fail("lse fill kernel launch", e);
+    if ((e = record(tm, false, 2, stream)) != cudaSuccess) return cuda_fail("cudaEventRecord", e);
+  }
 
   // Ring steps / chunks in order.  Their partials are independent of each other on one GPU
   // (every step reads only the inputs and writes its own plane), so consecutive steps share
@@ -948,7 +996,7 @@ slope_status slope_cp_prefill_timed(const slope_tensor* q, const slope_tensor* k
   if (q != nullptr && q->ndim == 3) {
     Plan plan;
     if (build_plan(q->shape[0], n_chunks, layout, chunk_sizes, causal, window, 0u, plan) == SLOPE_OK) {
-      int needed = 1;
+      int needed = 2;  // the lse fill and the merge
       size_t i = 0;
       for (int l = 0; l < plan.n_launches; ++l) {
         size_t c = 0;

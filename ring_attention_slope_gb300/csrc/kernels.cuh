@@ -91,6 +91,14 @@ struct MergeParams {
   int64_t lse_srow, lse_shead;
 };
 
+// -inf into whole fp32 lse planes: base + planes[i] * plane_elems, i < n.
+struct FillParams {
+  float* base;
+  int64_t plane_elems;
+  int32_t n;
+  int32_t planes[kMaxMerge];
+};
+
 // Status codes written into the device status word.
 constexpr int kStatusTimeout = 1;
 
@@ -103,6 +111,7 @@ cudaError_t launch_attn_partial(int dqk, int dv, const CUtensorMap& tq, const CU
                                 cudaStream_t stream);
 bool attn_partial_supported(int dqk, int dv);
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_lse_fill(const FillParams& p, cudaStream_t stream);
 // Head sizes the merge kernel is built for (64, 128 and 192).
 inline bool merge_dv_supported(long long dv) { return dv == 64 || dv == 128 || dv == 192; }
 cudaError_t launch_timeout_selftest(uint64_t limit_ns, int* status, cudaStream_t stream);

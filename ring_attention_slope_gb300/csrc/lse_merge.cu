@@ -13,6 +13,8 @@
 // writes bf16 or fp32.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "sm103_ptx.cuh"
 
@@ -146,7 +148,27 @@ cudaError_t launch_impl(const MergeParams& p, cudaStream_t stream) {
   return p.in_bf16 ? launch_in<DV, BF16, true>(p, stream) : launch_in<DV, BF16, false>(p, stream);
 }
 
+// Writes -inf into every element of the listed planes (coalesced 4-byte stores; each plane
+// is split over gridDim.x blocks, blockIdx.y picks the plane).
+__global__ void __launch_bounds__(256) lse_fill_kernel(const __grid_constant__ FillParams p) {
+  float* const plane = p.base + static_cast<int64_t>(p.planes[blockIdx.y]) * p.plane_elems;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.plane_elems; i += stride)
+    plane[i] = -INFINITY;
+}
+
 }  // namespace
+
+cudaError_t launch_lse_fill(const FillParams& p, cudaStream_t stream) {
+  if (p.n <= 0 || p.plane_elems <= 0) return cudaSuccess;
+  if (p.n > kMaxMerge) return cudaErrorInvalidValue;
+  // about 4 resident blocks per SM in total, split over the planes
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t per_plane = std::max<int64_t>(1, std::min<int64_t>((p.plane_elems + 255) / 256, (4LL * sms + p.n - 1) / p.n));
+  lse_fill_kernel<<<dim3(static_cast<unsigned>(per_plane), static_cast<unsigned>(p.n)), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_lse_merge(const MergeParams& p, cudaStream_t stream) {
   if (p.dv == 64) return p.out_bf16 ? launch_impl<64, true>(p, stream) : launch_impl<64, false>(p, stream);

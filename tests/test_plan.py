@@ -44,17 +44,33 @@ def test_ring_plan_covers_each_visible_pair_once(layout, N, window):
     assert n_launches == N and n_planes == N
     cnt, vis = coverage(items, S, window)
     assert np.array_equal(cnt, vis.astype(np.int32)), "some visible pair missing or counted twice"
-    # each step is one launch; in it every query row belongs to exactly one item (one partial per row and step)
+    # The key blocks each rank holds at step t, from the ring's definition (rank r holds the blocks of
+    # rank (r - t) mod N): a query row is in at most one item of step t, and a row in none sees no key
+    # of its rank's step-t blocks (its partial is the -inf lse written before the launches).
+    parts = 2 * N if layout == "zigzag" else N
+    sub = S // parts
+    owned = (lambda r: [r, 2 * N - 1 - r]) if layout == "zigzag" else (lambda r: [r])
+    owner = np.zeros(S, dtype=np.int64)
+    for r in range(N):
+        for c in owned(r):
+            owner[c * sub:(c + 1) * sub] = r
     for t in range(N):
         rows = np.zeros(S, dtype=np.int32)
         for it in items:
             if it["launch"] == t:
                 assert it["plane"] == t
                 rows[it["q_row0"]:it["q_row0"] + it["q_len"]] += 1
-        assert np.all(rows == 1)
-    # zigzag ownership: the ranks' query sub-chunks are r and 2N-1-r
+        assert np.all(rows <= 1)
+        held = np.zeros((S, S), dtype=bool)
+        for r in range(N):
+            keys = np.zeros(S, dtype=bool)
+            for c in owned((r - t) % N):
+                keys[c * sub:(c + 1) * sub] = True
+            held[owner == r] = keys
+        sees = (vis & held).any(axis=1)
+        assert not np.any(sees & (rows == 0)), "a row that sees a key of its step is in no item"
+    # zigzag ownership: the ranks' query sub-chunks are r and 2N-1-r (step 0 holds every diagonal)
     if layout == "zigzag":
-        sub = S // (2 * N)
         starts = sorted({it["q_row0"] // sub for it in items if it["launch"] == 0})
         assert starts == list(range(2 * N))
 
@@ -94,11 +110,18 @@ def test_chunked_plan(sizes, window):
     cnt, vis = coverage(items, S, window)
     assert np.array_equal(cnt, vis.astype(np.int32))
     starts = np.cumsum([0] + (sizes or [75] * 4))[:-1]
+    lens = sizes or [75] * 4
     for c in range(n):
         its = [it for it in items if it["launch"] == c]
-        assert sorted(it["plane"] for it in its) == [0, 1]
+        # the first chunk has no prefix to see, so no prefix partial; every other chunk's first rows see
+        # the tokens before it (with a window, only rows within the window of them do)
+        assert sorted(it["plane"] for it in its) == ([0, 1] if c > 0 else [1])
         for it in its:
-            assert it["q_row0"] == starts[c]
+            assert it["q_row0"] == starts[c] and 1 <= it["q_len"] <= lens[c]
+            if it["plane"] == 1 or window == 0:
+                assert it["q_len"] == lens[c]
+            else:
+                assert it["q_len"] == min(lens[c], window - 1)
             for k0, kl in it["kv"]:
                 if it["plane"] == 0:
                     assert k0 + kl <= starts[c]  # prefix partial: earlier tokens only
