@@ -46,8 +46,16 @@
  *    runs out records SLOPE_ERR_TIMEOUT in a device status word that
  *    slope_device_status() reports.
  *  - Calls are thread-safe (no mutable library state besides the device
- *    status word and a lazily resolved driver entry point).
+ *    status word, the work-tile counters below and a lazily resolved driver
+ *    entry point).
+ *  - Attention launches with dqk >= 128 (the MLA-shaped heads) claim their
+ *    work tiles at run time from a counter in static device memory, one of
+ *    SLOPE_TILE_COUNTERS per device handed out round robin, which every
+ *    launch leaves at 0 (also one whose CTAs found the status word set).
+ *    Launches on one stream never share one; across streams, keep fewer
+ *    than SLOPE_TILE_COUNTERS such launches queued or running at a time.
  */
+#define SLOPE_TILE_COUNTERS 4096
 #ifndef SLOPE_H
 #define SLOPE_H
 

@@ -21,7 +21,9 @@
 //   warps 9-10  MMA issuers, one per Q tile: S_t = Q_t K^T (SS, K-major) into
 //               TMEM, then O_t += P_t V (P from TMEM, V MN-major); warp 9 also
 //               owns the 512-column TMEM allocation.
-//   warp 11     idle.
+//   warp 11     idle, or, where tiles are claimed at run time, the scheduler: it takes the
+//               next work tile from the launch's global counter and hands its index to
+//               the other roles through one shared-memory word.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+dv), O_1 after it.
 // With dv = 64 the last 128 columns hold P_0 and P_1 (bf16 pairs, 64 columns
 // each), so the MMA warp issues S(n+1) = Q K(n+1)^T before O += P(n) V(n) and
@@ -48,6 +50,9 @@ namespace {
 constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 64 bf16 (128 bytes)
 constexpr int kTmaWarp = 4 * kQTiles;        // warps 0..7 are the two softmax warpgroups
 constexpr int kMmaWarp = kTmaWarp + 1;
+constexpr int kSchedWarp = kMmaWarp + kQTiles;  // warp 11
+// roles that read each claimed work tile: the TMA thread, the MMA issuers and the softmax warps
+constexpr int kTileReaders = 1 + kQTiles + 4 * kQTiles;
 // 12 warps put 3 warps on each SM sub-partition (16K registers each), which caps
 // a thread at 168 registers.
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -74,11 +79,18 @@ struct K1Cfg {
   static constexpr int kKTileBytes = kQChunks * kChunkBytes;
   static constexpr int kVTileBytes = kVChunks * kChunkBytes;
   static constexpr int kSlotBytes = kKTileBytes > kVTileBytes ? kKTileBytes : kVTileBytes;
+  // Work tiles claimed at run time from a global counter, in tile order, instead of the fixed
+  // w = blockIdx.x + k * gridDim.x.  Each CTA then takes the next tile when it has room for
+  // one, so the CTAs in flight always hold a window of about one grid's width of consecutive
+  // tiles: with one query head per KV head that keeps few heads' K/V in use at a time, which
+  // L2 holds, where the fixed order drifts apart (tile costs differ by row block) and spreads
+  // the CTAs over many heads.
+  static constexpr bool kDynamicTiles = DQK >= 128;
   // 128 KB of K/V slots: 8 of 16 KB at d = 64, 4 of 32 KB with a 128-column K or V tile, 2 of 48 KB at 192
   // (measured on the causal 32K zigzag workload: a second Q buffer, which leaves room for only
   // 6 slots at d = 64, cost 2.5%)
   static constexpr int kSlots = 131072 / kSlotBytes;
-  static constexpr int kNumBars = 1 + 2 * kSlots + 6 * kQTiles + 1 + 4 * kQTiles;
+  static constexpr int kNumBars = 1 + 2 * kSlots + 6 * kQTiles + 1 + 4 * kQTiles + (kDynamicTiles ? 2 : 0);
   // epilogue staging: 32-row x 32-column fp32 boxes (4 KB each, 128-byte swizzle), two per
   // softmax warp where shared memory allows (the second box is written while the first
   // one's store still reads), else one
@@ -262,6 +274,31 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const WorkItem*
   }
 }
 
+// Loop bounds of a CTA's work tiles: w = blockIdx.x, blockIdx.x + gridDim.x, ... in the fixed
+// order; with tiles claimed at run time the loop variable is set inside the loop instead.
+template <bool kDynamic>
+__device__ __forceinline__ int first_tile() {
+  return kDynamic ? 0 : static_cast<int>(blockIdx.x);
+}
+template <bool kDynamic>
+__device__ __forceinline__ int tile_stride() {
+  return kDynamic ? 0 : static_cast<int>(gridDim.x);
+}
+
+// For a CTA that computes no more tiles of a launch whose tiles are claimed at run time:
+// claims until an index past the end comes back, so that each CTA takes exactly one of those
+// (total .. total + gridDim.x - 1); the CTA handed the last one is the launch's last claim
+// and puts the counter back to 0 for the next launch that uses it.
+__device__ __forceinline__ void release_tiles(const AttnParams& p, int total) {
+  for (;;) {
+    const uint32_t w = atomicAdd(p.tile_counter, 1u);
+    if (w >= static_cast<uint32_t>(total)) {
+      if (w == static_cast<uint32_t>(total) + gridDim.x - 1) atomicExch(p.tile_counter, 0u);
+      return;
+    }
+  }
+}
+
 template <int DQK, int DV>
 __global__ void __launch_bounds__(kK1Threads, 1)
     attn_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -284,8 +321,11 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   uint64_t* bar_drain = bar_qempty + 1;  // one per MMA issuer
   uint64_t* bar_sfree = bar_drain + kQTiles;  // softmax t has loaded S_t into registers
   uint64_t* bar_turn = bar_sfree + kQTiles;    // [t * 4 + wq]: softmax warp (t, wq) may exponentiate
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_turn + 4 * kQTiles);
+  uint64_t* bar_tfull = bar_turn + 4 * kQTiles;  // the scheduler published the next work tile
+  uint64_t* bar_tfree = bar_tfull + 1;           // every reader has taken it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_turn + 4 * kQTiles + (C::kDynamicTiles ? 2 : 0));
   volatile int* cta_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* sTileIdx = reinterpret_cast<volatile int*>(tmem_slot + 2);  // claimed tile, -1 = none left
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = p.total_tiles;
@@ -299,6 +339,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   if (threadIdx.x == 0) *cta_abort = (*reinterpret_cast<volatile int*>(p.status) != 0) ? 1 : 0;
   __syncthreads();
   if (*cta_abort) {
+    if (C::kDynamicTiles && threadIdx.x == 0) release_tiles(p, total);
     pdl_wait();
     return;
   }
@@ -325,6 +366,10 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       mbar_init(&bar_sfree[t], 4);  // one arrival per softmax warp
       for (int q = 0; q < 4; ++q) mbar_init(&bar_turn[t * 4 + q], 1);  // lane 0 of the partner warp
     }
+    if (C::kDynamicTiles) {
+      mbar_init(bar_tfull, 1);
+      mbar_init(bar_tfree, kTileReaders);
+    }
     fence_barrier_init();
   }
   // work items into shared memory: dynamically indexed parameter reads miss the constant cache
@@ -346,14 +391,60 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint64_t limit = p.wait_limit_ns;
 
-  if (warp == kTmaWarp) {
+  // The tile loops run w = blockIdx.x, blockIdx.x + gridDim.x, ... (a fixed order), or, with
+  // tiles claimed at run time, take_tile() sets w at the top of each pass to the k-th tile the
+  // scheduler warp claimed (-1 after the last; false if the wait for it ran out) and the loop
+  // header only keeps the loop going.  `warp_wide`: the whole warp calls and lane 0 arrives.
+  auto take_tile = [&](int k, int& w, bool warp_wide) -> bool {
+    bool ok = wait_bounded(bar_tfull, k & 1, cta_abort, p.status, limit, 17);
+    if (warp_wide) ok = warp_all(ok);
+    if (!ok) return false;
+    w = *sTileIdx;
+    if (warp_wide) __syncwarp();
+    if (!warp_wide || lane == 0) mbar_arrive(bar_tfree);
+    return true;
+  };
+
+  if (C::kDynamicTiles && warp == kSchedWarp) {
+    // ================================================================ scheduler
+    // Claims work tiles one at a time: the next once every role has taken the previous one, so
+    // the CTA holds at most the tile it computes and the one it loads.  After the last tile (or
+    // once the CTA gave up on a wait) it still claims until it is handed an index past the end,
+    // so that every CTA takes exactly one of those and the counter can be put back to 0.
+    if (lane == 0) {
+      bool live = true;
+      for (int k = 0;; ++k) {
+        if (live && k > 0 && !wait_bounded(bar_tfree, (k - 1) & 1, cta_abort, p.status, limit, 18)) live = false;
+        if (!live) {
+          release_tiles(p, total);
+          break;
+        }
+        const uint32_t w = atomicAdd(p.tile_counter, 1u);
+        const bool end = w >= static_cast<uint32_t>(total);
+        *sTileIdx = end ? -1 : static_cast<int>(w);
+        mbar_arrive(bar_tfull);
+        if (end) {
+          if (w == static_cast<uint32_t>(total) + gridDim.x - 1) atomicExch(p.tile_counter, 0u);
+          break;
+        }
+      }
+    }
+  } else if (warp == kTmaWarp) {
     // ================================================================ TMA producer
     if (lane == 0) {
       uint32_t cnt = 0;
       int wt = 0;
       bool ok = true;
       int item_hint = 0;
-      for (int w = blockIdx.x; w < total; w += gridDim.x) {
+      int k = 0;
+      for (int w = first_tile<C::kDynamicTiles>(); w < total; w += tile_stride<C::kDynamicTiles>()) {
+        if constexpr (C::kDynamicTiles) {
+          if (!take_tile(k++, w, false)) {
+            ok = false;
+            break;
+          }
+          if (w < 0) break;
+        }
         Tile T;
         decode_tile<C::kGroupedTiles>(p, sItems, w, T, item_hint);
         if (!has_steps(T.itm, p, T.geo)) continue;
@@ -469,7 +560,15 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       bool ok = true;
       int wt = 0;
       int item_hint = 0;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      int k = 0;
+      for (int w = first_tile<C::kDynamicTiles>(); w < total && ok; w += tile_stride<C::kDynamicTiles>()) {
+        if constexpr (C::kDynamicTiles) {
+          if (!take_tile(k++, w, false)) {
+            ok = false;
+            break;
+          }
+          if (w < 0) break;
+        }
         Tile T;
         decode_tile<C::kGroupedTiles>(p, sItems, w, T, item_hint);
         if (!has_steps(T.itm, p, T.geo)) continue;
@@ -567,7 +666,15 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     int n = 0;  // steps (= PVs) of this Q tile over all work tiles
     bool ok = true;
     int item_hint = 0;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    int k = 0;
+    for (int w = first_tile<C::kDynamicTiles>(); w < total && ok; w += tile_stride<C::kDynamicTiles>()) {
+      if constexpr (C::kDynamicTiles) {
+        if (!take_tile(k++, w, true)) {
+          ok = false;
+          break;
+        }
+        if (w < 0) break;
+      }
       Tile T;
       decode_tile<C::kGroupedTiles>(p, sItems, w, T, item_hint);
       const int rows_t = t == 0 ? T.geo.rows[0] : T.geo.rows[1];
@@ -941,9 +1048,12 @@ int gcd_int(int a, int b) {
 // time.  When a KV head serves few query heads (Hq / Hkv < 4, as in MLA-shaped attention),
 // that is about one CTA per KV head, so each CTA streams its own K/V tiles from DRAM.  A group
 // of units just large enough to give the grid one group's row blocks puts many CTAs on the
-// same heads, and they then share those heads' K/V tiles in L2.  With larger GQA groups the
-// query heads of a KV head already share its tiles, and one group of all the units is kept.
-int tile_head_group(const AttnParams& p, long long grid) {
+// same heads, and they then share those heads' K/V tiles in L2.  With tiles claimed at run
+// time the CTAs in flight hold about one grid's width of consecutive tiles whatever the group,
+// and groups of one unit (an item's tiles head by head) put the fewest heads in that window.
+// With larger GQA groups the query heads of a KV head already share its tiles, and one group
+// of all the units is kept.
+int tile_head_group(const AttnParams& p, long long grid, bool dynamic_tiles) {
   int common = 0, max_blocks = 1;
   for (int i = 0; i < p.n_items; ++i) {
     common = gcd_int(common, p.items[i].h_count >> p.pair_heads);
@@ -951,6 +1061,7 @@ int tile_head_group(const AttnParams& p, long long grid) {
   }
   if (common <= 0) return 1;
   if (p.group >= 4) return common;
+  if (dynamic_tiles) return 1;
   const long long want = (grid + max_blocks - 1) / max_blocks;
   for (int hg = 1; hg < common; ++hg)
     if (common % hg == 0 && hg >= want) return hg;
@@ -969,7 +1080,11 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   p.total_tiles = static_cast<int32_t>(tiles);
   const long long grid = std::min<long long>(tiles, resident_ctas());
-  p.head_group = C::kGroupedTiles ? tile_head_group(p, grid) : 0;
+  p.head_group = C::kGroupedTiles ? tile_head_group(p, grid, C::kDynamicTiles) : 0;
+  if (C::kDynamicTiles) {
+    p.tile_counter = claim_tile_counter();
+    if (p.tile_counter == nullptr) return cudaErrorInvalidDevice;
+  }
   cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;

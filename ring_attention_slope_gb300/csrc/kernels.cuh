@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "slope.h"
+
 namespace slope {
 
 // ---------------------------------------------------------------- attention partial (K1)
@@ -65,6 +67,8 @@ struct AttnParams {
   float* lse;               // fp32 log-sum-exp planes
   int64_t lse_srow, lse_shead, lse_splane;
   int* status;              // device status word {code, site}
+  uint32_t* tile_counter;   // 0 at launch: work tiles claimed so far (kernels that claim them at run
+                            // time); set by the launcher
   uint64_t wait_limit_ns;   // bound on every barrier wait
   WorkItem items[kMaxItems];
 };
@@ -116,5 +120,9 @@ cudaError_t launch_lse_fill(const FillParams& p, cudaStream_t stream);
 inline bool merge_dv_supported(long long dv) { return dv == 64 || dv == 128 || dv == 192; }
 cudaError_t launch_timeout_selftest(uint64_t limit_ns, int* status, cudaStream_t stream);
 int* device_status_ptr();  // per current device; nullptr on failure
+// Work-tile counters for attention launches that claim tiles at run time (a ring in static device
+// memory, each 0 between launches).
+constexpr int kTileCounterSlots = SLOPE_TILE_COUNTERS;
+uint32_t* claim_tile_counter();  // the next counter of the current device; nullptr on failure
 
 }  // namespace slope

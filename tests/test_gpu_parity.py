@@ -5,6 +5,8 @@ relative L2 <= 5e-3, log-sum-exp max-abs <= 1e-3; rows that see no key must
 give exactly out = 0 and lse = -inf on both sides.
 """
 import math
+import os
+import re
 
 import numpy as np
 import pytest
@@ -74,6 +76,59 @@ def test_timeout_selftest_reports_and_context_survives():
     torch.cuda.synchronize()
     ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True)
     compare(out.cpu(), lse.cpu(), ro, rl, "after timeout self-test")
+    assert slope.device_status() == (0, 0)
+
+
+# ---------------------------------------------------------------- work tiles claimed at run time
+
+# The attention kernels for dqk >= 128 claim their work tiles from device counters that the
+# library hands out round robin, SLOPE_TILE_COUNTERS of them per device (each 0 between launches).
+TILE_COUNTERS = int(re.search(r"#define SLOPE_TILE_COUNTERS (\d+)",
+                              open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                                                "include", "slope.h")).read()).group(1))
+
+
+def test_claimed_tiles_same_bits_every_launch():
+    """Five MLA-shaped launches in a row, each claiming its tiles from the next counter (so CTAs take the
+    tiles in a different order each time): the same bits every time, and the oracle's values."""
+    q, k, v = qkv(1100, 6, 6, 192, 128, seed=31)
+    runs = []
+    for _ in range(5):
+        out, lse = slope.attn_partial(q, k, v, causal=True)
+        runs.append((out, lse))
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True)
+    compare(runs[0][0].cpu(), runs[0][1].cpu(), ro, rl, "claimed tiles")
+    for out, lse in runs[1:]:
+        assert torch.equal(out, runs[0][0]) and torch.equal(lse, runs[0][1])
+    assert slope.device_status() == (0, 0)
+
+
+def test_claimed_tile_counter_returns_to_zero_after_an_abort():
+    """A launch that starts while the status word holds an error computes nothing, yet its CTAs still claim
+    past the end and put the counter back to 0: every later launch, up to and past the one that reuses
+    that counter, computes every tile."""
+    S, H = 700, 4
+    q, k, v = qkv(S, H, H, 192, 128, seed=33)
+    out = torch.empty((S, H, 128), dtype=torch.float32, device="cuda")
+    lse = torch.empty((H, S), dtype=torch.float32, device="cuda")
+    ref_out, ref_lse = slope.attn_partial(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True)
+    compare(ref_out.cpu(), ref_lse.cpu(), ro, rl, "before the aborted launch")
+    slope.timeout_selftest(2_000_000)  # the status word now holds a timeout
+    slope.attn_partial(q, k, v, causal=True, out=out, lse=lse)  # its CTAs see it and return at once
+    st, site = slope.device_status()
+    assert st == -7 and site == 99
+    bad = torch.zeros((), dtype=torch.bool, device="cuda")
+    for _ in range(TILE_COUNTERS + 3):
+        out.fill_(math.nan)
+        lse.fill_(math.nan)
+        slope.attn_partial(q, k, v, causal=True, out=out, lse=lse)
+        bad |= ~(out == ref_out).all()  # a tile left uncomputed keeps its NaN
+        bad |= ~(lse == ref_lse).all()
+    torch.cuda.synchronize()
+    assert not bool(bad)
     assert slope.device_status() == (0, 0)
 
 
