@@ -251,7 +251,7 @@ def test_attn_partial_strided_views():
 # ---------------------------------------------------------------- merge
 
 @pytest.mark.parametrize("dv", [64, 128, 192])
-@pytest.mark.parametrize("n", [1, 2, 5, 16, 32])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 16, 32])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_lse_merge_matches_oracle(dv, n, out_dtype):
     S, H = 333, 6
