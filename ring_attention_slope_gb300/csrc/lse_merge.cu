@@ -27,14 +27,15 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // NMAX: compile-time bound on the number of partials (2, 4, 8, 16 or 32), so that the
 // per-thread log-sum-exp array fits in few registers when n is small and more warps stay
 // resident to hide the two dependent loads (lse, then partials): five blocks of 256 threads
-// per SM at n <= 4, four at n <= 8.  Measured on one GB300 against the old fixed bound of 32:
-// 2 partials 2.6 -> 6.8 TB/s, 8 partials 5.3 -> 6.7 TB/s, 16 partials 6.4 -> 7.0 TB/s; five
-// blocks instead of four at n <= 4 (no spills) took the merge of the 128-token-window ring
-// (three planes, most rows -inf in two of them) about 10% faster.
+// per SM at 3 or 4 partials, four at n <= 8 otherwise.  Measured on one GB300 against the old
+// fixed bound of 32: 2 partials 2.6 -> 6.8 TB/s, 8 partials 5.3 -> 6.7 TB/s, 16 partials
+// 6.4 -> 7.0 TB/s.  Five blocks instead of four (no spills) took the merge of the
+// 128-token-window ring (three planes, most rows -inf in two of them) from 0.80 to 0.88 of
+// the copy rate, but the two-plane merge of the chunked layout from 1.01 to 0.96.
 // IN_BF16: the partials are bf16 (each thread then reads 4 columns = 8 bytes per float4
 // position), halving the bytes read; accumulation stays fp32.
 template <int DV, bool OUT_BF16, int NMAX, bool IN_BF16>
-__global__ void __launch_bounds__(kMergeThreads, NMAX <= 4 ? 5 : NMAX <= 8 ? 4 : 2)
+__global__ void __launch_bounds__(kMergeThreads, NMAX == 4 ? 5 : NMAX <= 8 ? 4 : 2)
     lse_merge_kernel(const __grid_constant__ MergeParams p) {
   // DV/16 threads per (row, head), four float4 columns each: thread q owns float4
   // columns q, q+kTpp, q+2 kTpp, q+3 kTpp, so that each load instruction of a warp reads
