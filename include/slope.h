@@ -54,6 +54,8 @@
  *    launch leaves at 0 (also one whose CTAs found the status word set).
  *    Launches on one stream never share one; across streams, keep fewer
  *    than SLOPE_TILE_COUNTERS such launches queued or running at a time.
+ *    A launch recorded into a CUDA graph keeps the counter it was given for
+ *    every replay, so replays of one such graph must not overlap.
  */
 #define SLOPE_TILE_COUNTERS 4096
 #ifndef SLOPE_H
