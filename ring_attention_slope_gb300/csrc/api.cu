@@ -2,6 +2,7 @@
 // work decomposition of context-parallel prefill, TMA tensor maps and the
 // kernel launches.  The library allocates no device memory.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <atomic>
@@ -810,11 +811,22 @@ BufferSetEvents* buffer_set(int device, const void* key) {
 
 }  // namespace
 
+// One NVTX range around each public call that queues GPU work, named after the call, so that
+// Nsight tools group its launches (ncu --nvtx).  With no tool attached a push or pop is a check
+// of a function pointer.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+
 extern "C" {
 
 slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, const slope_tensor* v, int64_t q_off,
                                 int64_t kv_off, int causal, int64_t window, float scale, slope_tensor* out,
                                 slope_tensor* lse, void* stream) {
+  const CallRange range("slope_attn_partial");
   slope_status st;
   if ((st = check_qkv(q)) != SLOPE_OK) return st;
   if (k == nullptr || v == nullptr) return SLOPE_ERR_NULL;
@@ -894,6 +906,7 @@ slope_status slope_attn_partial(const slope_tensor* q, const slope_tensor* k, co
 
 slope_status slope_lse_merge(const slope_tensor* outs, const slope_tensor* lses, int n, slope_tensor* out,
                              slope_tensor* lse, void* stream) {
+  const CallRange range("slope_lse_merge");
   if (outs == nullptr || lses == nullptr || out == nullptr) return SLOPE_ERR_NULL;
   if (n < 1 || n > kMaxMerge) return SLOPE_ERR_SHAPE;
   if (out->ndim != 3) return SLOPE_ERR_SHAPE;
@@ -950,6 +963,7 @@ slope_status slope_cp_prefill(const slope_tensor* q, const slope_tensor* k, cons
                               slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
                               float scale, slope_tensor* out, slope_tensor* lse, void* workspace,
                               size_t workspace_bytes, void* stream) {
+  const CallRange range("slope_cp_prefill");
   return cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, 0u, out, lse, workspace,
                          workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
 }
@@ -958,6 +972,7 @@ slope_status slope_cp_prefill_ex(const slope_tensor* q, const slope_tensor* k, c
                                  slope_layout layout, const int64_t* chunk_sizes, int causal, int64_t window,
                                  float scale, unsigned flags, slope_tensor* out, slope_tensor* lse, void* workspace,
                                  size_t workspace_bytes, void* stream) {
+  const CallRange range("slope_cp_prefill_ex");
   return cp_prefill_impl(q, k, v, n_chunks, layout, chunk_sizes, causal, window, scale, flags, out, lse, workspace,
                          workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
 }
@@ -966,6 +981,7 @@ slope_status slope_cp_prefill_static_scratch(const slope_tensor* q, const slope_
                                              int n_chunks, slope_layout layout, const int64_t* chunk_sizes,
                                              int causal, int64_t window, float scale, slope_tensor* out,
                                              slope_tensor* lse, void* stream) {
+  const CallRange range("slope_cp_prefill_static_scratch");
   if (q == nullptr || v == nullptr) return SLOPE_ERR_NULL;
   if (q->ndim != 3 || v->ndim != 3) return SLOPE_ERR_SHAPE;
   const size_t need = slope_cp_prefill_workspace_size(q->shape[0], q->shape[1], v->shape[2], n_chunks, layout,
@@ -987,6 +1003,7 @@ slope_status slope_cp_prefill_timed(const slope_tensor* q, const slope_tensor* k
                                     int64_t window, float scale, slope_tensor* out, slope_tensor* lse,
                                     void* workspace, size_t workspace_bytes, void* stream, void** events,
                                     int n_event_pairs, int* n_launches, int* launch_kind) {
+  const CallRange range("slope_cp_prefill_timed");
   if (events == nullptr || n_launches == nullptr) return SLOPE_ERR_NULL;
   Timing tm;
   tm.events = events;
@@ -1019,6 +1036,7 @@ slope_status slope_cp_prefill_host(const slope_tensor* q_host, const slope_tenso
                                    const int64_t* chunk_sizes, int causal, int64_t window, float scale,
                                    void* workspace, size_t workspace_bytes, void* copy_in_stream,
                                    void* compute_stream, void* copy_out_stream) {
+  const CallRange range("slope_cp_prefill_host");
   if (q_host == nullptr || k_host == nullptr || v_host == nullptr || out_host == nullptr || q == nullptr ||
       k == nullptr || v == nullptr || out == nullptr)
     return SLOPE_ERR_NULL;
@@ -1129,6 +1147,7 @@ slope_status slope_device_status(void* stream, int* site) {
 }
 
 slope_status slope_debug_timeout_selftest(uint64_t limit_ns, void* stream) {
+  const CallRange range("slope_debug_timeout_selftest");
   if (limit_ns < 1000ull || limit_ns > 5000000000ull) return SLOPE_ERR_SHAPE;
   int* ptr = device_status_ptr();
   if (ptr == nullptr) return cuda_fail("device status word (cudaGetSymbolAddress)");
