@@ -10,8 +10,10 @@
 // by the log-sum-exp merge.  Over the whole sequence with bf16 output the same
 // launch is the complete attention (no partials, no merge).
 //
-// Persistent grid: one CTA per SM walks work tiles (one item x 256 query rows x
-// one query head), heaviest first; the launch's items sit in shared memory.
+// Persistent grid: one CTA per SM walks work tiles, heaviest first: one item x 128
+// query rows x two query heads of one KV group, or x 256 rows of one head.  At
+// d = 64 a CTA takes every gridDim.x-th tile; at dqk >= 128 the CTAs claim tiles
+// at run time.  The launch's items sit in shared memory.
 //   warps 0-3   online softmax of Q tile 0 (one query row per thread = TMEM lane),
 //   warps 4-7   online softmax of Q tile 1; each also runs its tile's epilogue,
 //               which stages O in shared memory (32-row x 128-byte boxes per
