@@ -390,20 +390,23 @@ def test_full_mla_s64k_chunked_var():
     check_full_workload(wl.WORKLOADS[4], 0)
 
 
-@pytest.mark.parametrize("layout,n", [("zigzag", 4), ("chunked", 3)])
-def test_cp_prefill_host_buffers_overlapped_calls(layout, n):
+@pytest.mark.parametrize("layout,n,dims", [("zigzag", 4, (8, 2, 64, 64)), ("chunked", 3, (8, 2, 64, 64)),
+                                           ("zigzag", 4, (4, 4, 192, 128))])
+def test_cp_prefill_host_buffers_overlapped_calls(layout, n, dims):
     """Three host-buffer prefills on two alternating device-buffer sets and three streams: each host
     result equals slope_cp_prefill on the same inputs, bit for bit (the third call reuses the first
-    call's device buffers while the second call's work may still run)."""
-    S, Hq, Hkv, d = 2048, 8, 2, 64
-    calls = [qkv(S, Hq, Hkv, d, d, seed=90 + i, device="cpu") for i in range(3)]
+    call's device buffers while the second call's work may still run).  With the MLA head sizes the
+    attention launches of overlapping calls claim their work tiles from separate counters."""
+    S = 2048
+    Hq, Hkv, d, dv = dims
+    calls = [qkv(S, Hq, Hkv, d, dv, seed=90 + i, device="cpu") for i in range(3)]
     hosts = [tuple(t.pin_memory() for t in c) for c in calls]
     sets = [dict(q=torch.empty(S, Hq, d, dtype=torch.bfloat16, device="cuda"),
                  k=torch.empty(S, Hkv, d, dtype=torch.bfloat16, device="cuda"),
-                 v=torch.empty(S, Hkv, d, dtype=torch.bfloat16, device="cuda"),
-                 out=torch.empty(S, Hq, d, dtype=torch.bfloat16, device="cuda"),
+                 v=torch.empty(S, Hkv, dv, dtype=torch.bfloat16, device="cuda"),
+                 out=torch.empty(S, Hq, dv, dtype=torch.bfloat16, device="cuda"),
                  lse=torch.empty(Hq, S, dtype=torch.float32, device="cuda")) for _ in range(2)]
-    houts = [torch.empty(S, Hq, d, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    houts = [torch.empty(S, Hq, dv, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
     hlses = [torch.empty(Hq, S, dtype=torch.float32).pin_memory() for _ in range(3)]
     s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ws = None
