@@ -50,11 +50,6 @@ namespace slope {
 namespace {
 
 constexpr uint32_t kChunkBytes = 128 * 128;  // 128 rows x 64 bf16 (128 bytes)
-constexpr int kTmaWarp = 4 * kQTiles;        // warps 0..7 are the two softmax warpgroups
-constexpr int kMmaWarp = kTmaWarp + 1;
-constexpr int kSchedWarp = kMmaWarp + kQTiles;  // warp 11
-// roles that read each claimed work tile: the TMA thread, the MMA issuers and the softmax warps
-constexpr int kTileReaders = 1 + kQTiles + 4 * kQTiles;
 // 12 warps put 3 warps on each SM sub-partition (16K registers each), which caps
 // a thread at 168 registers.
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -72,9 +67,23 @@ constexpr float kRescaleThreshold = 8.0f;    // log2 units
 // visible key rescales l and O by 0; a row that never sees a key writes 0.
 constexpr int kPolyPairsPer16 = 0;
 
-template <int DQK, int DV>
+// QT: Q tiles per CTA.  Two share every K/V tile and one CTA holds the SM (all 512 TMEM
+// columns, 12 warps); with one, two CTAs share the SM (256 columns and about 100 KB of shared
+// memory each, 6 warps each), and one CTA's work-tile boundary (last PV, epilogue, next Q load)
+// overlaps the other CTA's steps instead of stalling both Q tiles at once.
+template <int DQK, int DV, int QT = 2>
 struct K1Cfg {
   static_assert(DQK % 64 == 0 && DV % 64 == 0, "head dims are multiples of 64");
+  static_assert(QT == 1 || QT == 2, "one or two Q tiles per CTA");
+  static constexpr int kQTiles = QT;
+  static constexpr int kTmaWarp = 4 * QT;  // warps 0 .. 4 QT - 1 are the softmax warpgroups
+  static constexpr int kMmaWarp = kTmaWarp + 1;
+  static constexpr int kSchedWarp = kMmaWarp + QT;  // warp 11 with two Q tiles
+  // roles that read each claimed work tile: the TMA thread, the MMA issuers and the softmax warps
+  static constexpr int kTileReaders = 1 + QT + 4 * QT;
+  static constexpr int kThreads = QT == 2 ? 384 : 192;
+  static constexpr int kMinBlocks = QT == 2 ? 1 : 2;
+  static constexpr uint32_t kTmemCols = QT == 2 ? 512 : 256;
   static constexpr int kQChunks = DQK / 64;
   static constexpr int kVChunks = DV / 64;
   static constexpr int kQTileBytes = kQChunks * kChunkBytes;
@@ -90,24 +99,26 @@ struct K1Cfg {
   static constexpr bool kDynamicTiles = DQK >= 128;
   // 128 KB of K/V slots: 8 of 16 KB at d = 64, 4 of 32 KB with a 128-column K or V tile, 2 of 48 KB at 192
   // (measured on the causal 32K zigzag workload: a second Q buffer, which leaves room for only
-  // 6 slots at d = 64, cost 2.5%)
-  static constexpr int kSlots = 131072 / kSlotBytes;
-  static constexpr int kNumBars = 1 + 2 * kSlots + 6 * kQTiles + 1 + 4 * kQTiles + (kDynamicTiles ? 2 : 0);
+  // 6 slots at d = 64, cost 2.5%); 64 KB (4 slots at d = 64) with one Q tile per CTA
+  static constexpr int kSlots = (QT == 2 ? 131072 : 65536) / kSlotBytes;
+  static_assert(QT == 2 || !kDynamicTiles, "claimed tiles run with two Q tiles per CTA");
+  static constexpr int kNumBars = 1 + 2 * kSlots + 6 * QT + 1 + 4 * QT + (kDynamicTiles ? 2 : 0);
   // epilogue staging: 32-row x 32-column fp32 boxes (4 KB each, 128-byte swizzle), two per
   // softmax warp where shared memory allows (the second box is written while the first
   // one's store still reads), else one
-  static constexpr int kStageOffset = kQTiles * kQTileBytes + kSlots * kSlotBytes;
-  static constexpr int kStageBufs = kStageOffset + 2 * 4 * kQTiles * 4096 + 2048 <= 232448 ? 2 : 1;
-  static constexpr int kStageBytes = kStageBufs * 4 * kQTiles * 4096;
+  static constexpr int kStageOffset = QT * kQTileBytes + kSlots * kSlotBytes;
+  static constexpr int kStageBufs = QT == 2 && kStageOffset + 2 * 4 * QT * 4096 + 2048 <= 232448 ? 2 : 1;
+  static constexpr int kStageBytes = kStageBufs * 4 * QT * 4096;
   static constexpr int kBarOffset = kStageOffset + kStageBytes;
   // the launch's work items, copied from the kernel parameters (read on every work tile)
   static constexpr int kItemsOffset = kBarOffset + ((8 * kNumBars + 16 + 15) / 16) * 16;
   static constexpr int kSmemBytes = 1024 + kItemsOffset + kMaxItems * static_cast<int>(sizeof(WorkItem));
-  static constexpr uint32_t kColO = 256;
-  static constexpr uint32_t kColP = kColO + kQTiles * DV;           // separate P columns, if they fit
-  static constexpr bool kSepP = kColP + kQTiles * (kBlockN / 2) <= 512;
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kColO + kQTiles * DV <= 512, "TMEM budget");
+  static constexpr uint32_t kColO = QT * kBlockN;
+  static constexpr uint32_t kColP = kColO + QT * DV;  // separate P columns, if they fit
+  static constexpr bool kSepP = kColP + QT * (kBlockN / 2) <= kTmemCols;
+  // one CTA per SM, or two (each within half of the SM's 228 KB less 1 KB reserved per CTA)
+  static_assert(kSmemBytes <= (QT == 2 ? 232448 : 115712), "shared memory budget");
+  static_assert(kColO + QT * DV <= kTmemCols, "TMEM budget");
   // TMEM column of P_t
   __device__ static constexpr uint32_t col_p(int t) { return kSepP ? kColP + t * (kBlockN / 2) : t * kBlockN; }
   // The two softmax warps of an SM sub-partition take turns on their exponentials where P
@@ -142,10 +153,10 @@ struct Step {
 
 // Enumerates the K/V tiles of an item that at least one Q tile of this CTA can
 // see, in the same order for every role.  f returns false to stop (abort).
-template <typename F>
+template <int QT = kQTiles, typename F>
 __device__ __forceinline__ bool for_each_step(const WorkItem& it, const AttnParams& p, const TileGeom& g, F&& f) {
   const int qa_min = g.qa[0];
-  const int qb_max = g.rows[1] > 0 ? g.qb[1] : g.qb[0];
+  const int qb_max = QT == 2 && g.rows[1] > 0 ? g.qb[1] : g.qb[0];
   for (int r = 0; r < it.n_kv; ++r) {
     // select instead of a dynamic index: keeps the ranges in registers
     const int row0 = r == 0 ? it.kv[0].row0 : it.kv[1].row0;
@@ -163,7 +174,7 @@ __device__ __forceinline__ bool for_each_step(const WorkItem& it, const AttnPara
       s.part = 0;
       s.full = 0;
 #pragma unroll
-      for (int t = 0; t < kQTiles; ++t) {
+      for (int t = 0; t < QT; ++t) {
         if (g.rows[t] <= 0) continue;
         const bool vis = (!p.causal || s.kpos <= g.qb[t]) && (p.window == 0 || g.qa[t] - klast < p.window);
         if (!vis) continue;
@@ -209,9 +220,10 @@ __device__ __forceinline__ TileRange tile_range(int row0, int len, int qa, int q
 // without any (for example ring steps that a sliding window leaves empty) only need
 // their -inf log-sum-exp written by the softmax warps: the TMA and MMA warps skip them,
 // Q load and all, and count only the others in their Q-buffer phases.
+template <int QT = kQTiles>
 __device__ __forceinline__ bool has_steps(const WorkItem& it, const AttnParams& p, const TileGeom& g) {
   bool any = false;
-  for_each_step(it, p, g, [&](const Step&) -> bool {
+  for_each_step<QT>(it, p, g, [&](const Step&) -> bool {
     any = true;
     return false;
   });
@@ -231,8 +243,11 @@ struct Tile {
   TileGeom geo;
 };
 
-// First row (within the item) and head of Q tile t of a work tile.
+// First row (within the item) and head of Q tile t of a work tile (QT Q tiles per CTA; with one,
+// a work tile is 128 rows of one head).
+template <int QT>
 __device__ __forceinline__ int tile_row0(const AttnParams& p, const Tile& T, int t) {
+  if constexpr (QT == 1) return T.blk * kBlockM;
   return p.pair_heads ? T.blk * kBlockM : T.blk * kRowsPerCta + t * kBlockM;
 }
 __device__ __forceinline__ int tile_head(const AttnParams& p, const Tile& T, int t) {
@@ -246,7 +261,7 @@ __device__ __forceinline__ int tile_head(const AttnParams& p, const Tile& T, int
 // tiles in increasing w, so the item index never decreases and the scan resumes there.
 // kGrouped: tiles run unit group by unit group (p.head_group units each); otherwise every
 // unit of an item is inner to its row blocks.
-template <bool kGrouped>
+template <bool kGrouped, int QT>
 __device__ __forceinline__ void decode_tile(const AttnParams& p, const WorkItem* items, int w, Tile& T, int& ii) {
   const int ushift = p.pair_heads;  // head units per item = h_count >> ushift
   while (ii < p.n_items - 1 && w >= items[ii].tile_begin + items[ii].n_blocks * (items[ii].h_count >> ushift)) ++ii;
@@ -268,11 +283,16 @@ __device__ __forceinline__ void decode_tile(const AttnParams& p, const WorkItem*
   T.h = T.itm.h_begin + (unit << ushift);
   T.g = T.h / p.group;
 #pragma unroll
-  for (int t = 0; t < kQTiles; ++t) {
-    const int r0 = tile_row0(p, T, t);
+  for (int t = 0; t < QT; ++t) {
+    const int r0 = tile_row0<QT>(p, T, t);
     T.geo.rows[t] = max(0, min(kBlockM, T.itm.q_len - r0));
     T.geo.qa[t] = p.q_pos_off + T.itm.q_row0 + r0;
     T.geo.qb[t] = T.geo.qa[t] + T.geo.rows[t] - 1;
+  }
+  if constexpr (QT == 1) {  // the second slot of the geometry stays unused
+    T.geo.rows[1] = 0;
+    T.geo.qa[1] = T.geo.qa[0];
+    T.geo.qb[1] = T.geo.qb[0];
   }
 }
 
@@ -301,12 +321,14 @@ __device__ __forceinline__ void release_tiles(const AttnParams& p, int total) {
   }
 }
 
-template <int DQK, int DV>
-__global__ void __launch_bounds__(kK1Threads, 1)
+template <int DQK, int DV, int QT>
+__global__ void __launch_bounds__(K1Cfg<DQK, DV, QT>::kThreads, K1Cfg<DQK, DV, QT>::kMinBlocks)
     attn_partial_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                         const __grid_constant__ AttnParams p) {
-  using C = K1Cfg<DQK, DV>;
+  using C = K1Cfg<DQK, DV, QT>;
+  constexpr int kQTiles = C::kQTiles;  // Q tiles of this CTA
+  constexpr int kTmaWarp = C::kTmaWarp, kMmaWarp = C::kMmaWarp, kSchedWarp = C::kSchedWarp;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -347,7 +369,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   }
 
   if (warp == kMmaWarp) {
-    tmem_alloc(tmem_slot, 512);
+    tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
   if (threadIdx.x == kMmaWarp * 32) {
@@ -370,7 +392,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     }
     if (C::kDynamicTiles) {
       mbar_init(bar_tfull, 1);
-      mbar_init(bar_tfree, kTileReaders);
+      mbar_init(bar_tfree, C::kTileReaders);
     }
     fence_barrier_init();
   }
@@ -448,21 +470,21 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           if (w < 0) break;
         }
         Tile T;
-        decode_tile<C::kGroupedTiles>(p, sItems, w, T, item_hint);
-        if (!has_steps(T.itm, p, T.geo)) continue;
+        decode_tile<C::kGroupedTiles, C::kQTiles>(p, sItems, w, T, item_hint);
+        if (!has_steps<kQTiles>(T.itm, p, T.geo)) continue;
         // Q of the previous work tile is in use until its last S MMAs are done
         if (wt > 0 && !wait_bounded(bar_qempty, (wt - 1) & 1, cta_abort, p.status, limit, 11)) {
           ok = false;
           break;
         }
-        const int nq = T.geo.rows[1] > 0 ? 2 : 1;
+        const int nq = kQTiles == 2 && T.geo.rows[1] > 0 ? 2 : 1;
         mbar_arrive_expect_tx(bar_q, nq * C::kQTileBytes);
         for (int t = 0; t < nq; ++t)
           for (int c = 0; c < C::kQChunks; ++c)
             tma_load_3d(sQ + t * C::kQTileBytes + c * kChunkBytes, &tm_q, bar_q, 64 * c, tile_head(p, T, t),
-                        T.itm.q_row0 + tile_row0(p, T, t));
+                        T.itm.q_row0 + tile_row0<C::kQTiles>(p, T, t));
         ++wt;  // Q loads issued
-        ok = for_each_step(T.itm, p, T.geo, [&](const Step& s) -> bool {
+        ok = for_each_step<kQTiles>(T.itm, p, T.geo, [&](const Step& s) -> bool {
           {  // K tile
             const uint32_t slot = cnt % C::kSlots, ph = (cnt / C::kSlots) & 1;
             if (!wait_bounded(&bar_empty[slot], ph ^ 1, cta_abort, p.status, limit, 1)) return false;
@@ -494,7 +516,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+  } else if (warp == kMmaWarp || (kQTiles == 2 && warp == kMmaWarp + 1)) {
     // ================================================================ MMA issuers
     // One issuing thread per Q tile (warps on different SM sub-partitions), so each
     // tile's MMAs wait only on that tile's softmax.  Per step j issuer t issues
@@ -572,8 +594,8 @@ __global__ void __launch_bounds__(kK1Threads, 1)
           if (w < 0) break;
         }
         Tile T;
-        decode_tile<C::kGroupedTiles>(p, sItems, w, T, item_hint);
-        if (!has_steps(T.itm, p, T.geo)) continue;
+        decode_tile<C::kGroupedTiles, C::kQTiles>(p, sItems, w, T, item_hint);
+        if (!has_steps<kQTiles>(T.itm, p, T.geo)) continue;
         if (!wait_bounded(bar_q, wt & 1, cta_abort, p.status, limit, 3)) {
           ok = false;
           break;
@@ -581,7 +603,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         ++wt;
         tc_fence_after_sync();
         bool first = true;  // first PV of this work tile still due
-        ok = for_each_step(T.itm, p, T.geo, [&](const Step& s) -> bool {
+        ok = for_each_step<kQTiles>(T.itm, p, T.geo, [&](const Step& s) -> bool {
           const uint32_t kslot = cnt % C::kSlots, kph = (cnt / C::kSlots) & 1;
           ++cnt;
           const uint32_t vslot = cnt % C::kSlots, vph = (cnt / C::kSlots) & 1;
@@ -638,7 +660,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
     }
   } else if (warp < kTmaWarp) {
     // ================================================================ softmax + epilogue
-    const int t = warp >> 2;
+    const int t = kQTiles == 2 ? warp >> 2 : 0;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
@@ -678,12 +700,12 @@ __global__ void __launch_bounds__(kK1Threads, 1)
         if (w < 0) break;
       }
       Tile T;
-      decode_tile<C::kGroupedTiles>(p, sItems, w, T, item_hint);
+      decode_tile<C::kGroupedTiles, C::kQTiles>(p, sItems, w, T, item_hint);
       const int rows_t = t == 0 ? T.geo.rows[0] : T.geo.rows[1];
       // turns of this work tile: the step count of the tile with more steps
       int n_turns = 0;
       if (C::kTurns) {
-        int cnt[kQTiles] = {0, 0};
+        int cnt[2] = {0, 0};
 #pragma unroll
         for (int u = 0; u < kQTiles; ++u) {
           if (T.geo.rows[u] <= 0) continue;
@@ -871,7 +893,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
       // the wait for the tile's last PV.
       const bool valid_row = row < rows_t;
       const int head = tile_head(p, T, t);
-      const int64_t orow = static_cast<int64_t>(sit.out_row0) + tile_row0(p, T, t) + row;
+      const int64_t orow = static_cast<int64_t>(sit.out_row0) + tile_row0<C::kQTiles>(p, T, t) + row;
       const int64_t plane = sit.plane;
       if (valid_row) {
         p.lse[plane * p.lse_splane + orow * p.lse_srow + static_cast<int64_t>(head) * p.lse_shead] =
@@ -1018,7 +1040,7 @@ __global__ void __launch_bounds__(kK1Threads, 1)
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
   // Launched as a dependent of the previous attention launch, this grid finishes only after
   // that one has: a kernel queued after the last launch (the merge) then sees every launch's
@@ -1070,29 +1092,48 @@ int tile_head_group(const AttnParams& p, long long grid, bool dynamic_tiles) {
   return common;
 }
 
-template <int DQK, int DV>
+template <int DQK, int DV, int QT = 2>
 cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                         AttnParams p, bool dependent, cudaStream_t stream) {
-  using C = K1Cfg<DQK, DV>;
+  using C = K1Cfg<DQK, DV, QT>;
   if (p.n_items <= 0) return cudaSuccess;
-  const WorkItem& last = p.items[p.n_items - 1];
-  const long long tiles =
-      static_cast<long long>(last.tile_begin) + static_cast<long long>(last.n_blocks) * (last.h_count >> p.pair_heads);
+  long long tiles;
+  if constexpr (QT == 1) {
+    // one Q tile per CTA: work tiles of 128 rows of one head, counted here (the plan counts
+    // them for two Q tiles)
+    p.pair_heads = 0;
+    tiles = 0;
+    for (int i = 0; i < p.n_items; ++i) {
+      WorkItem& it = p.items[i];
+      it.n_blocks = (it.q_len + kBlockM - 1) / kBlockM;
+      if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+      it.tile_begin = static_cast<int32_t>(tiles);
+      tiles += static_cast<long long>(it.n_blocks) * it.h_count;
+    }
+  } else {
+    const WorkItem& last = p.items[p.n_items - 1];
+    tiles = static_cast<long long>(last.tile_begin) +
+            static_cast<long long>(last.n_blocks) * (last.h_count >> p.pair_heads);
+  }
   if (tiles <= 0) return cudaSuccess;
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   p.total_tiles = static_cast<int32_t>(tiles);
-  const long long grid = std::min<long long>(tiles, resident_ctas());
+  const long long grid = std::min<long long>(tiles, resident_ctas() * C::kMinBlocks);
   p.head_group = C::kGroupedTiles ? tile_head_group(p, grid, C::kDynamicTiles) : 0;
   if (C::kDynamicTiles) {
     p.tile_counter = claim_tile_counter();
     if (p.tile_counter == nullptr) return cudaErrorInvalidDevice;
   }
-  cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<DQK, DV, QT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  if constexpr (QT == 1) {  // the whole shared-memory carve-out, so that two CTAs fit on an SM
+    e = cudaFuncSetAttribute(attn_partial_kernel<DQK, DV, QT>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kK1Threads);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1100,7 +1141,7 @@ cudaError_t launch_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attn_partial_kernel<DQK, DV>, tq, tk, tv, to, p);
+  return cudaLaunchKernelEx(&cfg, attn_partial_kernel<DQK, DV, QT>, tq, tk, tv, to, p);
 }
 
 }  // namespace
@@ -1114,7 +1155,13 @@ bool attn_partial_supported(int dqk, int dv) {
 
 cudaError_t launch_attn_partial(int dqk, int dv, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& to, const AttnParams& p, bool dependent, cudaStream_t stream) {
-  if (dqk == 64 && dv == 64) return launch_impl<64, 64>(tq, tk, tv, to, p, dependent, stream);
+  if (dqk == 64 && dv == 64) {
+    // one Q tile per CTA and two CTAs per SM, except with a sliding window, whose two- or three-step
+    // work tiles run faster two to a CTA (measured: the causal 32K zigzag-8 ring +3.2%, the 32K
+    // single launch +8.3%, the 100K zigzag-16 ring +1.9%; the 100K window-128 ring -22%)
+    if (p.window > 0) return launch_impl<64, 64, 2>(tq, tk, tv, to, p, dependent, stream);
+    return launch_impl<64, 64, 1>(tq, tk, tv, to, p, dependent, stream);
+  }
   if (dqk == 64 && dv == 128) return launch_impl<64, 128>(tq, tk, tv, to, p, dependent, stream);
   if (dqk == 128 && dv == 64) return launch_impl<128, 64>(tq, tk, tv, to, p, dependent, stream);
   if (dqk == 128 && dv == 128) return launch_impl<128, 128>(tq, tk, tv, to, p, dependent, stream);

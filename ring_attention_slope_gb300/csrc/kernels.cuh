@@ -13,9 +13,8 @@ namespace slope {
 
 constexpr int kBlockM = 128;      // query rows per Q tile (= TMEM lanes)
 constexpr int kBlockN = 128;      // keys per K/V tile
-constexpr int kQTiles = 2;        // Q tiles per CTA; they share every K/V tile
-constexpr int kRowsPerCta = kBlockM * kQTiles;
-constexpr int kK1Threads = 384;   // warps 0..7 softmax (two warpgroups), 8 TMA, 9 MMA + TMEM owner, 10-11 idle
+constexpr int kQTiles = 2;        // Q tiles per CTA at most; a CTA's Q tiles share every K/V tile
+constexpr int kRowsPerCta = kBlockM * kQTiles;  // rows of a one-head work tile with two Q tiles
 constexpr int kMaxItems = 32;     // work items per launch
 constexpr int kMaxKvRanges = 2;   // key/value ranges per item
 
@@ -37,7 +36,8 @@ struct WorkItem {
   int32_t plane;       // output plane
   int32_t n_kv;        // 0..kMaxKvRanges
   int32_t tile_begin;  // first work tile of this item (prefix sum over items of n_blocks * head units)
-  int32_t n_blocks;    // ceil(q_len / rows per work tile): 128 with pair_heads, else kRowsPerCta
+  int32_t n_blocks;    // ceil(q_len / rows per work tile): 128 with pair_heads or one Q tile per
+                       // CTA (the launcher recounts for that kernel), else kRowsPerCta
   int32_t h_begin;     // first query head
   int32_t h_count;     // query heads (whole KV-head groups)
   KvRange kv[kMaxKvRanges];
