@@ -10,10 +10,13 @@
 // by the log-sum-exp merge.  Over the whole sequence with bf16 output the same
 // launch is the complete attention (no partials, no merge).
 //
-// Persistent grid: one CTA per SM walks work tiles, heaviest first: one item x 128
-// query rows x two query heads of one KV group, or x 256 rows of one head.  At
-// d = 64 a CTA takes every gridDim.x-th tile; at dqk >= 128 the CTAs claim tiles
-// at run time.  The launch's items sit in shared memory.
+// Persistent grid of CTAs that walk work tiles, heaviest first.  With two Q tiles per CTA
+// (windowed launches and dqk >= 128) one CTA holds an SM and a work tile is one item x 128
+// query rows x two query heads of one KV group, or x 256 rows of one head; with one Q tile
+// (d = 64 without a window) two CTAs share an SM, each with 6 warps (softmax 0-3, TMA 4,
+// MMA 5), 256 TMEM columns and half the shared memory, and a work tile is 128 rows of one
+// head.  At d = 64 a CTA takes every gridDim.x-th tile; at dqk >= 128 the CTAs claim tiles
+// at run time.  The launch's items sit in shared memory.  With two Q tiles:
 //   warps 0-3   online softmax of Q tile 0 (one query row per thread = TMEM lane),
 //   warps 4-7   online softmax of Q tile 1; each also runs its tile's epilogue,
 //               which stages O in shared memory (32-row x 128-byte boxes per
@@ -26,7 +29,8 @@
 //   warp 11     idle, or, where tiles are claimed at run time, the scheduler: it takes the
 //               next work tile from the launch's global counter and hands its index to
 //               the other roles through one shared-memory word.
-// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+dv), O_1 after it.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+dv), O_1 after it (one Q tile:
+// S [0,128), O [128,192), P [192,256)).
 // With dv = 64 the last 128 columns hold P_0 and P_1 (bf16 pairs, 64 columns
 // each), so the MMA warp issues S(n+1) = Q K(n+1)^T before O += P(n) V(n) and
 // the softmax of step n+1 starts while PV(n) still runs.  With dv = 128 TMEM is
