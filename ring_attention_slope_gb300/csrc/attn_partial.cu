@@ -11,9 +11,9 @@
 // launch is the complete attention (no partials, no merge).
 //
 // Persistent grid of CTAs that walk work tiles, heaviest first.  With two Q tiles per CTA
-// (windowed launches and dqk >= 128) one CTA holds an SM and a work tile is one item x 128
+// (windows up to 4096 keys, and dqk >= 128) one CTA holds an SM and a work tile is one item x 128
 // query rows x two query heads of one KV group, or x 256 rows of one head; with one Q tile
-// (d = 64 without a window) two CTAs share an SM, each with 6 warps (softmax 0-3, TMA 4,
+// (d = 64 otherwise) two CTAs share an SM, each with 6 warps (softmax 0-3, TMA 4,
 // MMA 5), 256 TMEM columns and half the shared memory, and a work tile is 128 rows of one
 // head.  At d = 64 a CTA takes every gridDim.x-th tile; at dqk >= 128 the CTAs claim tiles
 // at run time.  The launch's items sit in shared memory.  With two Q tiles:
@@ -1157,13 +1157,19 @@ bool attn_partial_supported(int dqk, int dv) {
   return (dqk == 64 || dqk == 128 || dqk == 192) && (dv == 64 || dv == 128);
 }
 
+// Windows up to this many keys run with two Q tiles per CTA at d = 64 (see launch_attn_partial).
+constexpr int kTwoTileMaxWindow = 4096;
+
 cudaError_t launch_attn_partial(int dqk, int dv, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& to, const AttnParams& p, bool dependent, cudaStream_t stream) {
   if (dqk == 64 && dv == 64) {
-    // one Q tile per CTA and two CTAs per SM, except with a sliding window, whose two- or three-step
-    // work tiles run faster two to a CTA (measured: the causal 32K zigzag-8 ring +3.2%, the 32K
-    // single launch +8.3%, the 100K zigzag-16 ring +1.9%; the 100K window-128 ring -22%)
-    if (p.window > 0) return launch_impl<64, 64, 2>(tq, tk, tv, to, p, dependent, stream);
+    // one Q tile per CTA and two CTAs per SM, except with a sliding window of up to 4096 keys, whose
+    // short work tiles run faster two to a CTA.  Measured: the causal 32K zigzag-8 ring +2.7%, the
+    // 32K single launch +7.2%, the 100K zigzag-16 ring +1.8%; the 100K window-128 ring -22%; on the
+    // 32K ring with windows of 128 .. 4096 keys the two-tile kernel leads by 28% .. 1%, at 8192 the
+    // one-tile kernel by 1%.
+    if (p.window > 0 && p.window <= kTwoTileMaxWindow)
+      return launch_impl<64, 64, 2>(tq, tk, tv, to, p, dependent, stream);
     return launch_impl<64, 64, 1>(tq, tk, tv, to, p, dependent, stream);
   }
   if (dqk == 64 && dv == 128) return launch_impl<64, 128>(tq, tk, tv, to, p, dependent, stream);
